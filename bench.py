@@ -1,0 +1,415 @@
+#!/usr/bin/env python
+"""Benchmark of the zero-copy host-resident KV-cache attention path on GB300.
+
+Default line: Llama-3-8B-shaped single-layer fused decode (B=8, 32/8 heads,
+head_dim 128, bf16, 32768 cached tokens per sequence in pinned, mapped host
+memory).  One step = one dkv_decode call (projection of the new token, append
+to the host cache, split-KV attention over the host-resident cache, combine).
+Lengths are reset between steps so every step appends at the same position.
+
+Reported alongside (same run, same process):
+  * the host-link read/write rate of a plain zero-copy streaming kernel (the
+    roofline denominator for the decode), the HBM read rate, cudaMemcpy H2D;
+  * two internal baselines on the same cache: naive untiled zero-copy
+    attention and copy-to-HBM-then-attend;
+  * the Llama-3-8B-shaped chunked prefill (T=4096 over a 28672-token prefix):
+    TFLOP/s against the min-of-rooflines bound;
+  * the fp64 CPU oracle timed on this host (a bounded sample).
+
+--impl reference times the CPU oracle (the only reference available for this
+method) on the same workload, metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from zero_copy_offloaded_gb300 import workloads as wl  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="dkv", choices=["dkv", "reference"])
+    ap.add_argument("--workload", default="llama8b_decode")
+    ap.add_argument("--prefill-workload", default="llama8b_prefill")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="only the headline decode (no baselines, prefill, oracle timing)")
+    ap.add_argument("--prefill-only", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return {}
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = max(mx, float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except Exception:
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- oracle
+def oracle_decode_sample(w: wl.Workload, seqs: int = 1):
+    """Time the fp64 oracle on `seqs` sequences of the decode workload."""
+    import oracle
+    oracle.set_threads(host_cores())
+    d = wl.make_dense(w.with_(B=seqs))
+    k = np.zeros((seqs, w.Hkv, w.S_max, w.D), np.uint16)
+    v = np.zeros_like(k)
+    wl.fill_cache(w.with_(B=seqs), k, v)
+    oracle.lib()
+    t0 = time.perf_counter()
+    oracle.step(d["x"], d["wq"], d["wk"], d["wv"], k, v, w.P, w.Hq, w.dtype)
+    dt = time.perf_counter() - t0
+    return dt, oracle.max_threads()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = wl.WORKLOADS[args.workload]
+    seqs = 1
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt, cores = oracle_decode_sample(w, seqs)
+        if i >= args.warmup:
+            times.append(dt)
+    tot = sum(times)
+    value = seqs * len(times) / tot
+    line = {
+        "impl": "reference", "metric": "fused KV-proj+attn decode tok/s", "value": value,
+        "unit": "tok/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "P": w.P, "H": w.H, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "D": w.D, "kv_dtype": w.dtype},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{seqs} of {w.B} sequences per step (all heads, P={w.P})"},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import zero_copy_offloaded_gb300 as dkv
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(v):
+        if not dist:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    pk = peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    w = wl.WORKLOADS[args.workload]
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+
+    def dev_tensor(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(tdt).to(dev)
+
+    # ------------------------------------------------ decode workload setup
+    cache = dkv.KVCache(w.B, w.Hkv, w.D, w.S_max, w.dtype)
+    wl.fill_cache(w, cache.k_host, cache.v_host)
+    dense = wl.make_dense(w)
+    x, wq, wk, wv = (dev_tensor(dense[k]) for k in ("x", "wq", "wk", "wv"))
+    x = x.reshape(w.B, 1, w.H)
+    out = torch.empty((w.B, 1, w.Hq, w.D), dtype=tdt, device=dev)
+    lens = np.full(w.B, w.P, np.int32)
+    dkv.dkv_cache_reserve(cache.h, w.Hq, 1)
+    dkv.dkv_cache_kernel_timing(cache.h, True)
+
+    def step():
+        cache.set_lengths(lens)
+        cache.decode(x, wq, wk, wv, w.Hq, out, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    cache.sync(stream)
+
+    # ------------------------------------------------ timed decode
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    clocks = Clocks(vis.split(",")[local] if vis else str(local))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    kern_ms = []
+    launches = 0
+    barrier()
+    clocks.start()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()  # L2 flush outside the timed events
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+        launches += dkv.dkv_last_launch_count()
+        kern_ms.append(dkv.dkv_cache_last_kernel_ms(cache.h))
+    barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    cache.sync(stream)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    tot_s = max_over_ranks(sum(step_ms) / 1e3)
+    value = w.B * args.steps * world / tot_s
+    fused_ms = statistics.mean(kern_ms)
+
+    # ------------------------------------------------ link / HBM probes
+    kd, vd = dkv.dkv_cache_device_ptrs(cache.h)
+    sink = torch.zeros(4, dtype=torch.int32, device=dev)
+    cache_bytes = w.B * w.Hkv * w.S_max * w.D * 2  # one of K / V
+
+    def time_kernel(fn, reps=5):
+        best = 1e30
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            best = min(best, a.elapsed_time(b))
+        return best
+
+    link_rd_ms = time_kernel(lambda: dkv.dkv_probe_read(kd, cache_bytes, sink, stream))
+    link_rd = cache_bytes / (link_rd_ms * 1e-3) / 1e9
+    pinned = torch.empty(256 << 20, dtype=torch.uint8, pin_memory=True)
+    link_wr_ms = time_kernel(lambda: dkv.dkv_probe_write(pinned.data_ptr(), pinned.numel(), stream))
+    link_wr = pinned.numel() / (link_wr_ms * 1e-3) / 1e9
+    hbm_buf = torch.empty(2 << 30, dtype=torch.uint8, device=dev)
+    hbm_ms = time_kernel(lambda: dkv.dkv_probe_read(hbm_buf, hbm_buf.numel(), sink, stream))
+    hbm_rd = hbm_buf.numel() / (hbm_ms * 1e-3) / 1e9
+    del hbm_buf
+    dst = torch.empty(pinned.numel(), dtype=torch.uint8, device=dev)
+    h2d_ms = time_kernel(lambda: dst.copy_(pinned, non_blocking=True))
+    h2d = pinned.numel() / (h2d_ms * 1e-3) / 1e9
+    del dst
+
+    host_bytes = w.host_read_bytes()
+    achieved = host_bytes / (fused_ms * 1e-3) / 1e9
+    roofline = {"bound": "host_link", "achieved": achieved, "peak": link_rd, "unit": "GB/s",
+                "frac": achieved / link_rd, "traffic": None,
+                "peak_source": "zero-copy streaming read probe over the same cache, same run",
+                "kernel": "decode_fused_kernel", "kernel_ms": fused_ms,
+                "algorithmic_bytes_per_launch": host_bytes}
+
+    # ------------------------------------------------ e2e through the C ABI with host buffers
+    x_host = torch.from_numpy(dense["x"].view(np.int16)).view(tdt).reshape(w.B, 1, w.H).pin_memory()
+    out_host = torch.empty(out.shape, dtype=tdt, pin_memory=True)
+    x_dev = torch.empty_like(x)
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        cache.set_lengths(lens)
+        cache.decode(x_dev, wq, wk, wv, w.Hq, out, stream)
+        out_host.copy_(out, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_val = w.B * len(e2e_ms) * world / max_over_ranks(sum(e2e_ms) / 1e3)
+
+    extras = {}
+    if not args.no_extras:
+        # naive untiled zero-copy attention and copy-to-HBM-then-attend, same cache
+        q = torch.randn((w.B, w.Hq, w.D), device=dev).to(tdt)
+        o2 = torch.empty_like(q)
+        cache.set_lengths(lens)
+        naive_ms = time_kernel(lambda: dkv.dkv_attend_naive(cache.h, q, w.Hq, o2, stream), reps=3)
+        ks = torch.empty(cache_bytes, dtype=torch.uint8, device=dev)
+        vs = torch.empty(cache_bytes, dtype=torch.uint8, device=dev)
+
+        def staged():
+            cache.set_lengths(lens)
+            dkv.dkv_decode_staged(cache.h, x, wq, wk, wv, w.H, w.Hq, out, ks, vs, stream)
+        staged_ms = time_kernel(staged, reps=3)
+        del ks, vs
+        extras["baselines"] = {
+            "fused_zero_copy_step_ms": statistics.mean(step_ms),
+            "naive_zero_copy_attention_ms": naive_ms,
+            "copy_to_hbm_then_attend_ms": staged_ms,
+            "hbm_staging_bytes": 2 * cache_bytes,
+        }
+        extras["prefill"] = bench_prefill(args, dkv, torch, dev, stream, flush, pk, link_rd,
+                                          link_wr, hbm_rd)
+    cache.free()
+
+    cpu = None
+    if rank == 0 and not args.no_extras:
+        dt, cores = oracle_decode_sample(w, 1)
+        cpu = {"value": 1.0 / dt, "unit": "tok/s", "cores": cores, "kind": "oracle",
+               "sample": f"1 of {w.B} sequences (all {w.Hq} heads, P={w.P}), one step"}
+
+    if rank == 0:
+        line = {
+            "metric": "fused KV-proj+attn decode tok/s", "value": value, "unit": "tok/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "P": w.P, "H": w.H, "Hq": w.Hq,
+                       "Hkv": w.Hkv, "D": w.D, "kv_cache": "pinned mapped host memory",
+                       "l2": "flushed between steps (256 MiB write outside the timed events)",
+                       "parallelism": f"replicas{world}"},
+            "host_link_gbs": host_bytes / (statistics.mean(step_ms) * 1e-3) / 1e9,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": "tok/s",
+                    "h2d_bytes_per_step": int(x_host.numel() * 2),
+                    "d2h_bytes_per_step": int(out_host.numel() * 2)},
+            "gpu_launches": launches,
+            "clocks": clk,
+            "link": {"zero_copy_read_gbs": link_rd, "zero_copy_write_gbs": link_wr,
+                     "memcpy_h2d_gbs": h2d, "hbm_read_gbs": hbm_rd,
+                     "hbm_measured_peak_gbs": pk.get("hbm_gbs")},
+            "wall_s_timed": wall,
+            **extras,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def bench_prefill(args, dkv, torch, dev, stream, flush, pk, link_rd, link_wr, hbm_rd):
+    w = wl.WORKLOADS[args.prefill_workload]
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+    cache = dkv.KVCache(w.B, w.Hkv, w.D, w.S_max, w.dtype)
+    wl.fill_cache(w, cache.k_host, cache.v_host)
+    dense = wl.make_dense(w)
+    x, wq, wk, wv = (torch.from_numpy(dense[k].view(np.int16)).view(tdt).to(dev)
+                     for k in ("x", "wq", "wk", "wv"))
+    out = torch.empty((w.B, w.T, w.Hq, w.D), dtype=tdt, device=dev)
+    lens = np.full(w.B, w.P, np.int32)
+    dkv.dkv_cache_reserve(cache.h, w.Hq, w.T)
+    dkv.dkv_cache_kernel_timing(cache.h, True)
+    times, kern = [], []
+    for i in range(5):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cache.set_lengths(lens)
+        a.record(stream)
+        cache.prefill(x, wq, wk, wv, w.Hq, out, stream)
+        b.record(stream)
+        b.synchronize()
+        if i >= 2:
+            times.append(a.elapsed_time(b))
+            kern.append(dkv.dkv_cache_last_kernel_ms(cache.h))
+    cache.sync(stream)
+    info = dkv.dkv_cache_info(cache.h)
+    cache.free()
+    ms = statistics.mean(times)
+    flops = w.flops()
+    tflops_peak = pk.get("bf16_tflops") or 1900.0
+    t_link_rd = w.host_read_bytes() / (link_rd * 1e9)
+    t_link_wr = w.host_write_bytes() / (link_wr * 1e9)
+    t_hbm = w.hbm_min_bytes() / (hbm_rd * 1e9)
+    t_flop = flops / (tflops_peak * 1e12)
+    t_roof = max(t_link_rd, t_link_wr, t_hbm, t_flop)
+    return {"workload": w.name, "ms": ms, "fused_kernel_ms": statistics.mean(kern),
+            "tflops": flops / (ms * 1e-3) / 1e12, "flops": flops,
+            "roofline_ms": t_roof * 1e3,
+            "roofline_terms_ms": {"link_read": t_link_rd * 1e3, "link_write": t_link_wr * 1e3,
+                                  "hbm": t_hbm * 1e3, "tensor": t_flop * 1e3},
+            "frac_of_roofline": t_roof / (ms * 1e-3),
+            "tensor_peak_tflops": tflops_peak,
+            "device_workspace_bytes": info["device_workspace_bytes"]}
+
+
+if __name__ == "__main__":
+    main()

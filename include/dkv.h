@@ -1,0 +1,195 @@
+/*
+ * dkv.h — C ABI of the zero-copy host-resident KV-cache attention library.
+ *
+ * The method is DirectKV ("No Buffer, No Bottleneck: Efficient Zero-Copy KV
+ * Cache Offloading for Long-Context LLMs").  Its pieces, as the pages
+ * describe them:
+ *   - KV Cache Manager: K/V tensors live in pinned host memory allocated with
+ *     cudaHostAlloc and are read by GPU kernels through zero-copy pointers;
+ *     once written they stay there across decode iterations ("Paper Notes:
+ *     DirectKV", System Architecture, KV Cache Manager).
+ *   - Attention Fusion Engine: one kernel computes the K/V projection of the
+ *     new token(s), keeps the fresh K/V on chip and runs attention over the
+ *     host-resident cache (same page, System Architecture and Key Ideas (2)).
+ *     Prefill iterates over HBM-resident Q for each host K/V tile; decode
+ *     iterates over all cached K/V for the single new query (same page,
+ *     System Architecture, prefill/decode strategies).
+ *   - CPU-memory-aware tiling: a host K/V tile is fetched once and reused by
+ *     every query tile and head that needs it (same page, Key Ideas (1)).
+ *   - Kernel Adaptor: picks a precompiled kernel by dtype, head dim, tile and
+ *     phase (same page, System Architecture, Kernel Adaptor).
+ * The attention computed is softmax(Q.K^T / sqrt(d)).V with K = X.Wk,
+ * V = X.Wv (same page, Fundamental Underlying Technologies, Kernel Fusion).
+ *
+ * Conventions for every call:
+ *   - Shapes: B batch, T new tokens per sequence, H hidden, Hq query heads,
+ *     Hkv KV heads (Hq a multiple of Hkv; query head h uses KV head
+ *     h / (Hq/Hkv)), D head dim.
+ *   - x is [B, T, H]; Wq is [H, Hq*D]; Wk and Wv are [H, Hkv*D]; out is
+ *     [B, T, Hq, D]; all row-major, all in the cache's dtype, all DEVICE
+ *     pointers owned by the caller.
+ *   - The K cache and the V cache are each [B][Hkv][max_tokens][D] in pinned,
+ *     mapped host memory owned by the library.
+ *   - A stream argument is a cudaStream_t passed as void* (NULL = the legacy
+ *     default stream).  Work is enqueued; nothing waits for the GPU unless
+ *     the call says so.
+ *   - No call throws.  Argument, capacity and support errors return before
+ *     anything is enqueued and leave the cache unchanged.  dkv_last_error()
+ *     gives a thread-local detail string for the last failure.
+ */
+#ifndef DKV_H
+#define DKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DKV_OK = 0,
+    DKV_ERR_INVALID_ARG = 1,      /* null pointer, bad size, bad handle */
+    DKV_ERR_UNSUPPORTED = 2,      /* no precompiled kernel for (dtype, D, G) */
+    DKV_ERR_CAPACITY = 3,         /* length + T would exceed max_tokens */
+    DKV_ERR_NO_MAPPED_MEMORY = 4, /* the device cannot map host memory */
+    DKV_ERR_ALLOC = 5,            /* pinned host or device allocation failed */
+    DKV_ERR_CUDA = 6,             /* a CUDA runtime call failed */
+    DKV_ERR_TIMEOUT = 7           /* a bounded device-side wait gave up */
+} dkv_status;
+
+typedef enum { DKV_BF16 = 0, DKV_FP16 = 1 } dkv_dtype;
+
+typedef struct dkv_cache dkv_cache; /* opaque; tagged so a stale handle is rejected */
+
+/* Sizes of what a cache holds (the pages' memory accounting: zero bytes of
+ * HBM staging; "Paper Notes: DirectKV", Experiments, GPU memory). */
+typedef struct {
+    size_t host_pinned_bytes;  /* K + V caches in pinned, mapped host memory */
+    size_t device_workspace_bytes; /* library-owned HBM for q, fresh K/V, partials */
+    size_t device_staging_bytes;   /* HBM copies of the cache: always 0 */
+    int batch, n_kv_heads, head_dim, max_tokens, dtype;
+} dkv_cache_info_t;
+
+/* Allocate a K cache and a V cache of [batch][n_kv_heads][max_tokens][head_dim]
+ * elements each with cudaHostAlloc(Mapped | Portable) and obtain their device
+ * aliases with cudaHostGetDevicePointer (KV Cache Manager, "Paper Notes:
+ * DirectKV", System Architecture).  Sequence lengths start at 0.  The current
+ * CUDA device is the one the cache serves.  Host contents are zeroed.
+ * Errors: INVALID_ARG (null out, non-positive size, dtype), UNSUPPORTED
+ * (head_dim not 64 or 128), NO_MAPPED_MEMORY (device cannot map host
+ * memory), ALLOC. */
+dkv_status dkv_cache_alloc(dkv_cache** out, int batch, int n_kv_heads, int head_dim,
+                           int max_tokens, dkv_dtype dtype);
+
+/* Release the pinned caches and the device workspace.  The caller must make
+ * sure no enqueued work still uses the cache.  A handle already freed (or
+ * never returned by dkv_cache_alloc) gives INVALID_ARG. */
+dkv_status dkv_free(dkv_cache* cache);
+
+/* Host addresses of the two caches ([B][Hkv][max_tokens][D] each), for
+ * filling prefixes and reading back appended rows.  The host must not touch
+ * rows that enqueued work reads or writes until that work has finished. */
+dkv_status dkv_cache_host_ptrs(dkv_cache* cache, void** k_host, void** v_host);
+
+/* Device aliases of the same two caches (zero-copy pointers). */
+dkv_status dkv_cache_device_ptrs(dkv_cache* cache, void** k_dev, void** v_dev);
+
+/* Set / read the per-sequence lengths (cached rows per sequence), len[B].
+ * Set: INVALID_ARG if a length is negative, CAPACITY if above max_tokens. */
+dkv_status dkv_cache_set_lengths(dkv_cache* cache, const int32_t* len);
+dkv_status dkv_cache_get_lengths(const dkv_cache* cache, int32_t* len);
+
+dkv_status dkv_cache_info(const dkv_cache* cache, dkv_cache_info_t* info);
+
+/* Reserve the device workspace for calls with up to n_q_heads query heads and
+ * up to max_new_tokens new tokens per sequence, so that later calls allocate
+ * nothing.  Without it the first call of a larger shape grows the workspace
+ * (a cudaMalloc on the calling thread, after synchronising the cache's last
+ * stream). */
+dkv_status dkv_cache_reserve(dkv_cache* cache, int n_q_heads, int max_new_tokens);
+
+/* One decode step (T = 1) for every sequence: q = x.Wq, k = x.Wk, v = x.Wv
+ * (fp32 accumulation in sequential order over H, rounded to the dtype), the
+ * new k, v appended at row len[b] of the host cache, then softmax attention
+ * of the Hq query heads over keys 0..len[b] of their KV head (the new token
+ * included), written to out [B, 1, Hq, D].  Lengths advance by 1 when the
+ * call is enqueued.  One cooperative launch of the fused kernel plus a
+ * split-KV combine launch.  Errors: INVALID_ARG, UNSUPPORTED (dtype, D,
+ * Hq/Hkv), CAPACITY, ALLOC (workspace growth), CUDA.  Device-side wait
+ * timeouts are reported by dkv_sync_status. */
+dkv_status dkv_decode(dkv_cache* cache, const void* x, const void* wq, const void* wk,
+                      const void* wv, int hidden, int n_q_heads, void* out, void* stream);
+
+/* One prefill (chunked-prefill) call: T new tokens per sequence at rows
+ * [len[b], len[b]+T).  Query t of sequence b (absolute position len[b]+t)
+ * attends causally to keys 0..len[b]+t.  Q = x.Wq is written to HBM first
+ * (Q is HBM-resident, "Paper Notes: DirectKV", System Architecture, prefill
+ * strategy); the fused kernel then holds each host K/V chunk stationary in
+ * shared memory, computing the fresh K/V rows of chunks in the new region
+ * in place and appending them to the host cache, and runs every query tile
+ * of the KV head against it; a combine launch merges the per-chunk partial
+ * results.  out is [B, T, Hq, D].  Lengths advance by T when enqueued.
+ * Errors as dkv_decode. */
+dkv_status dkv_prefill(dkv_cache* cache, const void* x, int T, const void* wq, const void* wk,
+                       const void* wv, int hidden, int n_q_heads, void* out, void* stream);
+
+/* Synchronise the stream, then return and clear the device status word that
+ * bounded waits write (DKV_ERR_TIMEOUT), or DKV_ERR_CUDA if the stream
+ * reported an error. */
+dkv_status dkv_sync_status(dkv_cache* cache, void* stream);
+
+/* Tuning overrides for ablations; 0 keeps the adaptor's choice.
+ *   splits       decode: key-range splits per (sequence, KV head)
+ *   tile_n       keys per host tile (decode) or per stationary chunk (prefill)
+ *   stages       decode ring depth m */
+dkv_status dkv_cache_set_tuning(dkv_cache* cache, int splits, int tile_n, int stages);
+
+const char* dkv_status_str(dkv_status s);
+const char* dkv_last_error(void);
+
+/* ---- measurement kernels (internal baselines and link probes) ----------- */
+
+/* Stream `bytes` (a multiple of 16) from `src` (a device pointer: a mapped
+ * host alias for the link, HBM for the HBM rate) with 16-byte loads across
+ * the whole GPU; the folded sum goes to sink[0] (device, 16 bytes) so the
+ * loads cannot be elided.  The plain zero-copy streaming kernel whose rate is
+ * the host-link denominator of the roofline. */
+dkv_status dkv_probe_read(const void* src, size_t bytes, void* sink, void* stream);
+
+/* Write `bytes` (a multiple of 16) of a pattern to `dst` with 16-byte stores. */
+dkv_status dkv_probe_write(void* dst, size_t bytes, void* stream);
+
+/* Naive untiled zero-copy decode attention (the pages' "naive zero-copy"
+ * baseline, "Paper Notes: DirectKV", Experiments, CPU-aware tiling): one CTA
+ * per (sequence, query head, split) reads its KV head's rows straight from
+ * the host cache with no shared-memory tile and no reuse across the heads of
+ * a group.  It attends q (HBM, [B, Hq, D], the dtype) over keys 0..len[b]-1
+ * of the cache as it stands (no projection, no append) into out [B, Hq, D]. */
+dkv_status dkv_attend_naive(dkv_cache* cache, const void* q, int n_q_heads, void* out,
+                            void* stream);
+
+/* Copy-to-HBM-then-attend baseline (swap-style staging, "Paper Notes:
+ * DirectKV", Motivation): cudaMemcpyAsync the cached rows [0, len[b]) of
+ * every (sequence, KV head) into the caller's HBM buffers k_stage, v_stage
+ * (each [B][Hkv][max_tokens][D]) and run the same fused decode as dkv_decode
+ * reading the prefix from HBM (the append still goes to the host cache). */
+dkv_status dkv_decode_staged(dkv_cache* cache, const void* x, const void* wq, const void* wk,
+                             const void* wv, int hidden, int n_q_heads, void* out,
+                             void* k_stage, void* v_stage, void* stream);
+
+/* Kernel timing for measurement: when enabled, each dkv_decode / dkv_prefill
+ * records a pair of CUDA events on its stream around its main fused kernel
+ * (not the projection or combine launches).  dkv_cache_last_kernel_ms waits
+ * for the last recorded pair and returns its elapsed time in milliseconds;
+ * INVALID_ARG if timing is off or nothing was recorded yet. */
+dkv_status dkv_cache_kernel_timing(dkv_cache* cache, int enable);
+dkv_status dkv_cache_last_kernel_ms(dkv_cache* cache, float* ms);
+
+/* Number of kernel launches the last dkv_decode / dkv_prefill enqueued. */
+int dkv_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DKV_H */

@@ -1,0 +1,113 @@
+"""Shared test plumbing: build a cache from a seeded workload, run the CUDA
+path through the C ABI, run the oracle on the same inputs, compare."""
+from __future__ import annotations
+
+import numpy as np
+
+from zero_copy_offloaded_gb300 import workloads as wl
+
+# Tolerances on the attention output versus the fp64 oracle: maximum absolute
+# error and sum|gpu - ref| / sum|ref|.
+MAX_ABS = 1e-2
+MEAN_REL = 2e-3
+
+
+def torch_dtype(dtype):
+    import torch
+    return torch.bfloat16 if dtype == "bf16" else torch.float16
+
+
+def to_dev(bits: np.ndarray, dtype):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch_dtype(dtype)).cuda()
+
+
+def to_bits(t) -> np.ndarray:
+    import torch
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def out_f64(t, dtype) -> np.ndarray:
+    import oracle
+    return oracle.decode_bits(to_bits(t), dtype)
+
+
+def errors(got: np.ndarray, ref: np.ndarray):
+    d = np.abs(got - ref)
+    return float(d.max()), float(d.sum() / max(np.abs(ref).sum(), 1e-300))
+
+
+def assert_close(got, ref, what=""):
+    mx, mr = errors(got, ref)
+    assert mx <= MAX_ABS and mr <= MEAN_REL, f"{what}: max_abs={mx:.3e} mean_rel={mr:.3e}"
+    return mx, mr
+
+
+class Case:
+    """A workload materialised on the GPU and in the host cache."""
+
+    def __init__(self, w: wl.Workload, lens=None, s_max=None, tuning=None):
+        import zero_copy_offloaded_gb300 as dkv
+        self.w = w
+        self.dense = wl.make_dense(w)
+        self.s_max = s_max or w.S_max
+        self.lens = np.broadcast_to(np.asarray(w.P if lens is None else lens, np.int64),
+                                    (w.B,)).copy()
+        self.cache = dkv.KVCache(w.B, w.Hkv, w.D, self.s_max, w.dtype)
+        # prefix rows: the workload's generator, truncated per sequence
+        kc = np.zeros((w.B, w.Hkv, self.s_max, w.D), np.uint16)
+        vc = np.zeros_like(kc)
+        wp = w.with_(P=int(self.lens.max()))
+        for b in range(w.B):
+            for h in range(w.Hkv):
+                kk, vv = wl.cache_slice(wp, b, h)
+                n = int(self.lens[b])
+                kc[b, h, :n] = kk[:n]
+                vc[b, h, :n] = vv[:n]
+        # canary pattern beyond the prefix: must be overwritten only by appends
+        kc[:, :, :, :][np.broadcast_to(np.arange(self.s_max)[None, None, :, None]
+                                       >= self.lens[:, None, None, None], kc.shape)] = 0x7E57
+        vc[np.broadcast_to(np.arange(self.s_max)[None, None, :, None]
+                           >= self.lens[:, None, None, None], vc.shape)] = 0x7E57
+        self.cache.k_host[...] = kc
+        self.cache.v_host[...] = vc
+        self.k0, self.v0 = kc, vc
+        self.cache.set_lengths(self.lens.astype(np.int32))
+        if tuning:
+            dkv.dkv_cache_set_tuning(self.cache.h, **tuning)
+        self.x = to_dev(self.dense["x"], w.dtype)
+        self.wq = to_dev(self.dense["wq"], w.dtype)
+        self.wk = to_dev(self.dense["wk"], w.dtype)
+        self.wv = to_dev(self.dense["wv"], w.dtype)
+
+    def out_tensor(self, T):
+        import torch
+        w = self.w
+        return torch.empty((w.B, T, w.Hq, w.D), dtype=torch_dtype(w.dtype), device="cuda")
+
+    def run_decode(self, x=None):
+        out = self.out_tensor(1)
+        x = self.x if x is None else x
+        self.cache.decode(x.reshape(self.w.B, 1, self.w.H), self.wq, self.wk, self.wv, self.w.Hq,
+                          out)
+        self.cache.sync()
+        return out
+
+    def run_prefill(self, x=None):
+        x = self.x if x is None else x
+        out = self.out_tensor(x.shape[1])
+        self.cache.prefill(x, self.wq, self.wk, self.wv, self.w.Hq, out)
+        self.cache.sync()
+        return out
+
+    def oracle(self, x_bits=None, rows=None, k=None, v=None, lens=None):
+        import oracle
+        w = self.w
+        return oracle.step(self.dense["x"] if x_bits is None else x_bits, self.dense["wq"],
+                           self.dense["wk"], self.dense["wv"], self.k0 if k is None else k,
+                           self.v0 if v is None else v, self.lens if lens is None else lens,
+                           w.Hq, w.dtype, rows=rows)
+
+    def free(self):
+        self.cache.free()

@@ -1,0 +1,111 @@
+"""Prefill parity: Q projection + fused KV-stationary prefill + combine
+(through the C ABI) against the fp64 oracle on the same seeded inputs.
+
+Bars as for decode: appended K/V rows equal the oracle's fp32-sequential
+projection rounded to the dtype (bit-exact while the projection is an fp32
+chain over H in order); attention output max-abs <= 1e-2 and
+sum|err|/sum|ref| <= 2e-3 versus fp64; prefix rows and rows past the
+append untouched."""
+import numpy as np
+import pytest
+
+from zero_copy_offloaded_gb300 import workloads as wl
+
+from .helpers import Case, assert_close, out_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def check_prefill(case: Case, out, ref, label="", rows=None):
+    w = case.w
+    T = out.shape[1]
+    got = out_f64(out, w.dtype).reshape(w.B, T, w.Hq, w.D)
+    if rows is None:
+        res = assert_close(got, ref["out"], label)
+    else:
+        g = np.stack([got[b, t] for (b, t) in rows])
+        r = np.stack([ref["out"][(b, t)] for (b, t) in rows])
+        res = assert_close(g, r, label)
+    kh, vh = case.cache.k_host, case.cache.v_host
+    for b in range(w.B):
+        p = int(case.lens[b])
+        assert np.array_equal(kh[b, :, p:p + T], ref["k_new"][b].transpose(1, 0, 2)), f"{label} k"
+        assert np.array_equal(vh[b, :, p:p + T], ref["v_new"][b].transpose(1, 0, 2)), f"{label} v"
+        assert np.array_equal(kh[b, :, :p], case.k0[b, :, :p])
+        assert np.array_equal(vh[b, :, :p], case.v0[b, :, :p])
+        assert np.all(kh[b, :, p + T:] == 0x7E57) and np.all(vh[b, :, p + T:] == 0x7E57)
+    return res
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 8, 2), (64, 4, 4), (128, 8, 1), (64, 16, 2)])
+@pytest.mark.parametrize("P,T", [(0, 1), (0, 37), (5, 300), (300, 17), (600, 129)])
+def test_prefill_shapes(dtype, D, Hq, Hkv, P, T):
+    w = wl.Workload("t", "prefill", B=2, H=128, Hq=Hq, Hkv=Hkv, D=D, P=P, T=T, dtype=dtype,
+                    kv_dist="uniform2" if dtype == "fp16" else "normal", seed=P + T)
+    case = Case(w, s_max=P + T + 3)
+    try:
+        out = case.run_prefill()
+        check_prefill(case, out, case.oracle(), f"{dtype} D{D} G{Hq // Hkv} P{P} T{T}")
+    finally:
+        case.free()
+
+
+def test_prefill_ragged_lengths():
+    w = wl.Workload("t", "prefill", B=3, H=64, Hq=8, Hkv=2, D=128, P=520, T=40, seed=4)
+    case = Case(w, lens=[0, 520, 257], s_max=600)
+    try:
+        out = case.run_prefill()
+        check_prefill(case, out, case.oracle(), "ragged")
+        assert list(case.cache.lengths()) == [40, 560, 297]
+    finally:
+        case.free()
+
+
+def test_prefill_then_decode_matches_oracle():
+    w = wl.Workload("t", "prefill", B=1, H=128, Hq=8, Hkv=2, D=64, P=100, T=64, seed=8)
+    case = Case(w, s_max=200)
+    try:
+        out = case.run_prefill()
+        ref = case.oracle()
+        check_prefill(case, out, ref, "prefill")
+        from .helpers import to_dev
+        x2 = wl.make_dense(w.with_(T=1, seed=99))["x"]
+        out2 = case.run_decode(to_dev(x2, w.dtype))
+        ref2 = case.oracle(x_bits=x2, k=ref["k_cache_after"], v=ref["v_cache_after"],
+                           lens=case.lens + w.T)
+        got = out_f64(out2, w.dtype).reshape(w.B, w.Hq, w.D)
+        assert_close(got, ref2["out"].reshape(w.B, w.Hq, w.D), "decode after prefill")
+    finally:
+        case.free()
+
+
+@pytest.mark.slow
+def test_prefill_mha_fp16_full_size():
+    """fp16 MHA prefill workload at full size (B=2, T=2048 over P=6144)."""
+    w = wl.WORKLOADS["mha_fp16_prefill"]
+    case = Case(w)
+    try:
+        out = case.run_prefill()
+        rng = np.random.default_rng(0)
+        rows = [(b, t) for b in range(w.B) for t in [0, 1, w.T - 1] + list(rng.integers(0, w.T, 20))]
+        check_prefill(case, out, case.oracle(rows=rows), "mha_fp16_prefill", rows=rows)
+    finally:
+        case.free()
+
+
+@pytest.mark.slow
+def test_prefill_llama8b_full_size_sampled_rows():
+    """Llama-3-8B-shaped chunked prefill at full size (T=4096 over P=28672);
+    every appended row is checked, attention on a seeded sample of query rows
+    (first, last, chunk edges and random)."""
+    w = wl.WORKLOADS["llama8b_prefill"]
+    case = Case(w)
+    try:
+        out = case.run_prefill()
+        rng = np.random.default_rng(0)
+        ts = sorted(set([0, 1, 255, 256, 2047, w.T - 1] + list(rng.integers(0, w.T, 26))))
+        rows = [(0, int(t)) for t in ts]
+        check_prefill(case, out, case.oracle(rows=rows), "llama8b_prefill", rows=rows)
+    finally:
+        case.free()

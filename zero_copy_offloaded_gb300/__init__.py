@@ -1,0 +1,277 @@
+"""Zero-copy host-resident KV-cache attention for GB300 (DirectKV's hot path).
+
+A thin ctypes binding over ``libdkv.so`` whose C ABI is ``include/dkv.h``.
+Every function here only marshals arguments (tensor -> device pointer,
+stream -> cudaStream_t) and calls the library of the same name; every step
+of the computation runs in the library's CUDA kernels.  There is no CPU or
+PyTorch fallback: if the library is missing or a call fails, a
+``DkvError`` is raised.
+
+PyTorch is used only as plumbing for device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+__all__ = [
+    "DkvError", "BF16", "FP16", "lib", "lib_path", "KVCache",
+    "dkv_cache_alloc", "dkv_free", "dkv_cache_host_ptrs", "dkv_cache_device_ptrs",
+    "dkv_cache_set_lengths", "dkv_cache_get_lengths", "dkv_cache_info", "dkv_cache_reserve",
+    "dkv_cache_set_tuning", "dkv_decode", "dkv_prefill", "dkv_sync_status", "dkv_status_str",
+    "dkv_last_error", "dkv_probe_read", "dkv_probe_write", "dkv_attend_naive",
+    "dkv_decode_staged", "dkv_last_launch_count", "dkv_cache_kernel_timing",
+    "dkv_cache_last_kernel_ms",
+]
+
+BF16 = 0
+FP16 = 1
+_DTYPE = {"bf16": BF16, "fp16": FP16, BF16: BF16, FP16: FP16}
+STATUS = {0: "DKV_OK", 1: "DKV_ERR_INVALID_ARG", 2: "DKV_ERR_UNSUPPORTED", 3: "DKV_ERR_CAPACITY",
+          4: "DKV_ERR_NO_MAPPED_MEMORY", 5: "DKV_ERR_ALLOC", 6: "DKV_ERR_CUDA",
+          7: "DKV_ERR_TIMEOUT"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "_build", "libdkv.so")
+
+
+class DkvError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+        super().__init__(f"{where}: {self.name}: {detail}")
+
+
+class _CacheInfo(ctypes.Structure):
+    _fields_ = [("host_pinned_bytes", ctypes.c_size_t),
+                ("device_workspace_bytes", ctypes.c_size_t),
+                ("device_staging_bytes", ctypes.c_size_t),
+                ("batch", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("max_tokens", ctypes.c_int),
+                ("dtype", ctypes.c_int)]
+
+
+_lib = None
+
+
+def lib(build_if_missing: bool = False):
+    """The loaded libdkv (built in-tree by ``zero_copy_offloaded_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise ImportError(f"{path} is missing: run zero_copy_offloaded_gb300/build.py "
+                              "(the CUDA library is required; there is no fallback)")
+        from . import build as _b
+        _b.build()
+    L = ctypes.CDLL(path)
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "dkv_cache_alloc": [ctypes.POINTER(P), I, I, I, I, I],
+        "dkv_free": [P],
+        "dkv_cache_host_ptrs": [P, ctypes.POINTER(P), ctypes.POINTER(P)],
+        "dkv_cache_device_ptrs": [P, ctypes.POINTER(P), ctypes.POINTER(P)],
+        "dkv_cache_set_lengths": [P, P],
+        "dkv_cache_get_lengths": [P, P],
+        "dkv_cache_info": [P, ctypes.POINTER(_CacheInfo)],
+        "dkv_cache_reserve": [P, I, I],
+        "dkv_cache_set_tuning": [P, I, I, I],
+        "dkv_decode": [P, P, P, P, P, I, I, P, P],
+        "dkv_prefill": [P, P, I, P, P, P, I, I, P, P],
+        "dkv_sync_status": [P, P],
+        "dkv_probe_read": [P, Z, P, P],
+        "dkv_probe_write": [P, Z, P],
+        "dkv_attend_naive": [P, P, I, P, P],
+        "dkv_decode_staged": [P, P, P, P, P, I, I, P, P, P, P],
+        "dkv_cache_kernel_timing": [P, I],
+        "dkv_cache_last_kernel_ms": [P, ctypes.POINTER(ctypes.c_float)],
+    }
+    for name, args in sig.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
+    L.dkv_status_str.argtypes = [ctypes.c_int]
+    L.dkv_status_str.restype = ctypes.c_char_p
+    L.dkv_last_error.argtypes = []
+    L.dkv_last_error.restype = ctypes.c_char_p
+    L.dkv_last_launch_count.argtypes = []
+    L.dkv_last_launch_count.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise DkvError(st, where, lib().dkv_last_error().decode())
+
+
+def _ptr(t) -> int | None:
+    """Device pointer of a CUDA tensor (or an int / None passed through)."""
+    if t is None or isinstance(t, int):
+        return t
+    if hasattr(t, "data_ptr"):
+        if not t.is_contiguous():
+            raise ValueError("tensor must be contiguous")
+        return t.data_ptr()
+    raise TypeError(f"cannot take a device pointer of {type(t)}")
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def dkv_status_str(st: int) -> str:
+    return lib().dkv_status_str(st).decode()
+
+
+def dkv_last_error() -> str:
+    return lib().dkv_last_error().decode()
+
+
+def dkv_last_launch_count() -> int:
+    return lib().dkv_last_launch_count()
+
+
+def dkv_cache_alloc(batch, n_kv_heads, head_dim, max_tokens, dtype="bf16") -> int:
+    h = ctypes.c_void_p()
+    _check(lib().dkv_cache_alloc(ctypes.byref(h), batch, n_kv_heads, head_dim, max_tokens,
+                                 _DTYPE[dtype]), "dkv_cache_alloc")
+    return h.value
+
+
+def dkv_free(h):
+    _check(lib().dkv_free(h), "dkv_free")
+
+
+def dkv_cache_host_ptrs(h):
+    k, v = ctypes.c_void_p(), ctypes.c_void_p()
+    _check(lib().dkv_cache_host_ptrs(h, ctypes.byref(k), ctypes.byref(v)), "dkv_cache_host_ptrs")
+    return k.value, v.value
+
+
+def dkv_cache_device_ptrs(h):
+    k, v = ctypes.c_void_p(), ctypes.c_void_p()
+    _check(lib().dkv_cache_device_ptrs(h, ctypes.byref(k), ctypes.byref(v)),
+           "dkv_cache_device_ptrs")
+    return k.value, v.value
+
+
+def dkv_cache_set_lengths(h, lens):
+    a = np.ascontiguousarray(lens, dtype=np.int32)
+    _check(lib().dkv_cache_set_lengths(h, a.ctypes.data), "dkv_cache_set_lengths")
+
+
+def dkv_cache_get_lengths(h, batch):
+    a = np.zeros(batch, np.int32)
+    _check(lib().dkv_cache_get_lengths(h, a.ctypes.data), "dkv_cache_get_lengths")
+    return a
+
+
+def dkv_cache_info(h) -> dict:
+    i = _CacheInfo()
+    _check(lib().dkv_cache_info(h, ctypes.byref(i)), "dkv_cache_info")
+    return {f: getattr(i, f) for f, _ in _CacheInfo._fields_}
+
+
+def dkv_cache_reserve(h, n_q_heads, max_new_tokens):
+    _check(lib().dkv_cache_reserve(h, n_q_heads, max_new_tokens), "dkv_cache_reserve")
+
+
+def dkv_cache_set_tuning(h, splits=0, tile_n=0, stages=0):
+    _check(lib().dkv_cache_set_tuning(h, splits, tile_n, stages), "dkv_cache_set_tuning")
+
+
+def dkv_cache_kernel_timing(h, enable=True):
+    _check(lib().dkv_cache_kernel_timing(h, int(bool(enable))), "dkv_cache_kernel_timing")
+
+
+def dkv_cache_last_kernel_ms(h) -> float:
+    ms = ctypes.c_float()
+    _check(lib().dkv_cache_last_kernel_ms(h, ctypes.byref(ms)), "dkv_cache_last_kernel_ms")
+    return float(ms.value)
+
+
+def dkv_decode(h, x, wq, wk, wv, hidden, n_q_heads, out, stream=None):
+    _check(lib().dkv_decode(h, _ptr(x), _ptr(wq), _ptr(wk), _ptr(wv), hidden, n_q_heads,
+                            _ptr(out), _stream(stream)), "dkv_decode")
+
+
+def dkv_prefill(h, x, T, wq, wk, wv, hidden, n_q_heads, out, stream=None):
+    _check(lib().dkv_prefill(h, _ptr(x), T, _ptr(wq), _ptr(wk), _ptr(wv), hidden, n_q_heads,
+                             _ptr(out), _stream(stream)), "dkv_prefill")
+
+
+def dkv_sync_status(h, stream=None):
+    _check(lib().dkv_sync_status(h, _stream(stream)), "dkv_sync_status")
+
+
+def dkv_probe_read(src, nbytes, sink, stream=None):
+    _check(lib().dkv_probe_read(_ptr(src), nbytes, _ptr(sink), _stream(stream)), "dkv_probe_read")
+
+
+def dkv_probe_write(dst, nbytes, stream=None):
+    _check(lib().dkv_probe_write(_ptr(dst), nbytes, _stream(stream)), "dkv_probe_write")
+
+
+def dkv_attend_naive(h, q, n_q_heads, out, stream=None):
+    _check(lib().dkv_attend_naive(h, _ptr(q), n_q_heads, _ptr(out), _stream(stream)),
+           "dkv_attend_naive")
+
+
+def dkv_decode_staged(h, x, wq, wk, wv, hidden, n_q_heads, out, k_stage, v_stage, stream=None):
+    _check(lib().dkv_decode_staged(h, _ptr(x), _ptr(wq), _ptr(wk), _ptr(wv), hidden, n_q_heads,
+                                   _ptr(out), _ptr(k_stage), _ptr(v_stage), _stream(stream)),
+           "dkv_decode_staged")
+
+
+class KVCache:
+    """Owner of one dkv_cache handle, with numpy views of the pinned caches."""
+
+    def __init__(self, batch, n_kv_heads, head_dim, max_tokens, dtype="bf16"):
+        self.B, self.Hkv, self.D, self.S_max = batch, n_kv_heads, head_dim, max_tokens
+        self.dtype = dtype
+        self.h = dkv_cache_alloc(batch, n_kv_heads, head_dim, max_tokens, dtype)
+        kp, vp = dkv_cache_host_ptrs(self.h)
+        shape = (batch, n_kv_heads, max_tokens, head_dim)
+        n = int(np.prod(shape))
+        self.k_host = np.ctypeslib.as_array((ctypes.c_uint16 * n).from_address(kp)).reshape(shape)
+        self.v_host = np.ctypeslib.as_array((ctypes.c_uint16 * n).from_address(vp)).reshape(shape)
+
+    def set_lengths(self, lens):
+        dkv_cache_set_lengths(self.h, np.broadcast_to(np.asarray(lens, np.int32), (self.B,)))
+
+    def lengths(self):
+        return dkv_cache_get_lengths(self.h, self.B)
+
+    def decode(self, x, wq, wk, wv, n_q_heads, out, stream=None):
+        dkv_decode(self.h, x, wq, wk, wv, x.shape[-1], n_q_heads, out, stream)
+
+    def prefill(self, x, wq, wk, wv, n_q_heads, out, stream=None):
+        dkv_prefill(self.h, x, x.shape[1], wq, wk, wv, x.shape[-1], n_q_heads, out, stream)
+
+    def sync(self, stream=None):
+        dkv_sync_status(self.h, stream)
+
+    def free(self):
+        if self.h is not None:
+            self.k_host = self.v_host = None
+            dkv_free(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass

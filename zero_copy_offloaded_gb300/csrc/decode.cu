@@ -1,0 +1,548 @@
+// Fused decode: projection + append + split-KV attention over a host-resident
+// KV cache read zero-copy, then the split-KV combine.
+//
+// DirectKV's decode strategy iterates over all cached (K, V) for the single
+// new query ("Paper Notes: DirectKV", System Architecture, Attention Fusion
+// Engine); K/V projection and attention run in one kernel with the fresh K/V
+// kept on chip (Key Ideas (2)); producer warps fetch the next host tile while
+// consumer warps compute on the current one (Key Ideas (3)); each host tile
+// is read once and reused by every query head of its KV group (Key Ideas (1)).
+//
+// GB300 design: one persistent cooperative launch, one CTA per SM.
+//   Phase A  every CTA projects a slice of the [Wq | Wk | Wv] columns for all
+//            sequences (fp32 FMA chain over H in order, rounded once), writes
+//            q and the fresh k/v to a small HBM workspace and appends k/v to
+//            the host cache.  Meanwhile the producer warps already stream the
+//            CTA's first host tiles into the shared-memory ring.
+//   barrier  bounded grid-wide arrival counter (co-residency is guaranteed by
+//            the cooperative launch).
+//   Phase B  units (sequence b, KV head, key-range split) in a static
+//            round-robin.  Producer warps copy host K/V tiles with 16-byte
+//            cp.async into an m-stage ring (mbarrier hand-off); consumer warps
+//            compute the G heads' scores, the online softmax and P.V in fp32
+//            and write one normalised partial (o, lse) per unit.
+// The combine kernel merges the splits with a log-sum-exp weighting.
+#include "dkv_internal.cuh"
+
+namespace dkv {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kProducerWarps = 2;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kProducers = kProducerWarps * 32;
+constexpr int kThreads = kConsumers + kProducers;
+constexpr int kBarConsumers = 1;  // named barrier id for the consumer warps
+constexpr int kProjRows = 128;    // H rows per projection chunk
+constexpr int kProjCols = 64;     // columns per projection pass (multiple of 8)
+
+// Shared-memory layout (byte offsets), all derived from the launch shape.
+struct DecodeSmem {
+  int ring, bars, q, s, alpha, ml, red, wproj, xproj, flag, total;
+  __host__ __device__ DecodeSmem(int D, int G, int N, int stages, int B) {
+    int tile_bytes = N * D * 2;
+    int off = 0;
+    ring = off; off += stages * 2 * tile_bytes;
+    bars = off; off += 2 * stages * 8;
+    q = off; off += G * (D + 4) * 4;
+    s = off; off += 2 * G * N * 4;
+    alpha = off; off += 2 * G * 4;
+    ml = off; off += 2 * G * 4;
+    red = off; off += kConsumers * 2 * 4;
+    off = (off + 15) & ~15;
+    wproj = off; off += 2 * kProjRows * kProjCols * 2;
+    xproj = off; off += 2 * B * kProjRows * 2;
+    flag = off; off += 16;
+    total = off;
+  }
+};
+
+template <typename T, int D>
+__device__ __forceinline__ const T* col_source(const DecodeParams& p, int col, int& which,
+                                               int& local) {
+  const int nq = p.Hq * D, nk = p.Hkv * D;
+  if (col < nq) { which = 0; local = col; return static_cast<const T*>(p.wq); }
+  if (col < nq + nk) { which = 1; local = col - nq; return static_cast<const T*>(p.wk); }
+  which = 2; local = col - nq - nk; return static_cast<const T*>(p.wv);
+}
+
+// Phase A: columns [c_begin, c_end) of [Wq | Wk | Wv] for all B sequences.
+// Each output is one fp32 FMA chain over j = 0..H-1 in order (each product of
+// two 16-bit floats is exact in fp32, so the chain equals summing the exact
+// products with one fp32 rounding per step), rounded once to T.
+template <typename T, int D>
+__device__ void project_columns(const DecodeParams& p, int c_begin, int c_end, uint8_t* smem,
+                                const DecodeSmem& L, int ctid) {
+  T* wbuf = reinterpret_cast<T*>(smem + L.wproj);   // [2][kProjRows][kProjCols]
+  T* xbuf = reinterpret_cast<T*>(smem + L.xproj);   // [2][B][kProjRows]
+  const T* x = static_cast<const T*>(p.x);
+  const int B = p.B, H = p.H;
+  const int nchunks = (H + kProjRows - 1) / kProjRows;
+  for (int cb = c_begin; cb < c_end; cb += kProjCols) {
+    const int ncols = min(kProjCols, c_end - cb);  // multiple of 8
+    const int npairs = ncols / 2;
+    const int nbp = (B + 1) / 2;
+    const int ngroups = npairs * nbp;
+    for (int gbase = 0; gbase < ngroups; gbase += kConsumers) {
+      const int gi = gbase + ctid;
+      const bool active = gi < ngroups;
+      const int pair = active ? gi % npairs : 0;
+      const int b0 = active ? (gi / npairs) * 2 : 0;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+
+      auto issue = [&](int chunk, int buf) {
+        const int j0 = chunk * kProjRows;
+        const int rows = min(kProjRows, H - j0);
+        const int pieces_per_row = ncols / 8;
+        T* wdst = wbuf + buf * kProjRows * kProjCols;
+        for (int i = ctid; i < rows * pieces_per_row; i += kConsumers) {
+          const int r = i / pieces_per_row, pc = i % pieces_per_row;
+          int which, local;
+          const T* base = col_source<T, D>(p, cb + pc * 8, which, local);
+          const int width = which == 0 ? p.Hq * D : p.Hkv * D;
+          cp_async16(wdst + r * kProjCols + pc * 8, base + (size_t)(j0 + r) * width + local, 16);
+        }
+        T* xdst = xbuf + buf * B * kProjRows;
+        const int xpieces = rows / 8;
+        for (int i = ctid; i < B * xpieces; i += kConsumers) {
+          const int b = i / xpieces, pc = i % xpieces;
+          cp_async16(xdst + b * kProjRows + pc * 8, x + (size_t)b * H + j0 + pc * 8, 16);
+        }
+        cp_async_commit();
+      };
+
+      issue(0, 0);
+      for (int c = 0; c < nchunks; ++c) {
+        if (c + 1 < nchunks) {
+          issue(c + 1, (c + 1) & 1);
+          cp_async_wait_group<1>();
+        } else {
+          cp_async_wait_group<0>();
+        }
+        named_bar_sync(kBarConsumers, kConsumers);
+        if (active) {
+          const int rows = min(kProjRows, H - c * kProjRows);
+          const T* wsrc = wbuf + (c & 1) * kProjRows * kProjCols;
+          const T* xs = xbuf + (c & 1) * B * kProjRows;
+          const bool two = b0 + 1 < B;
+#pragma unroll 4
+          for (int j = 0; j < rows; ++j) {
+            const uint32_t w2 = *reinterpret_cast<const uint32_t*>(wsrc + j * kProjCols + pair * 2);
+            const float2 w = DT<T>::to_f2(w2);
+            const float xa = DT<T>::to_f(xs[b0 * kProjRows + j]);
+            acc[0] = fmaf(xa, w.x, acc[0]);
+            acc[1] = fmaf(xa, w.y, acc[1]);
+            if (two) {
+              const float xb = DT<T>::to_f(xs[(b0 + 1) * kProjRows + j]);
+              acc[2] = fmaf(xb, w.x, acc[2]);
+              acc[3] = fmaf(xb, w.y, acc[3]);
+            }
+          }
+        }
+        named_bar_sync(kBarConsumers, kConsumers);
+      }
+      if (active) {
+        const int col = cb + pair * 2;
+        int which, local;
+        (void)col_source<T, D>(p, col, which, local);
+        for (int bb = 0; bb < 2; ++bb) {
+          const int b = b0 + bb;
+          if (b >= B) break;
+          T v0 = DT<T>::from_f(acc[bb * 2]), v1 = DT<T>::from_f(acc[bb * 2 + 1]);
+          if (which == 0) {
+            T* q = static_cast<T*>(p.q_ws) + (size_t)b * p.Hq * D + local;
+            q[0] = v0; q[1] = v1;
+          } else {
+            const int kvh = local / D, d = local % D;
+            T* ws = static_cast<T*>(p.kv_ws) + ((size_t)b * 2 + (which - 1)) * p.Hkv * D + local;
+            ws[0] = v0; ws[1] = v1;
+            T* host = static_cast<T*>(which == 1 ? p.k_host : p.v_host) +
+                      (((size_t)b * p.Hkv + kvh) * p.S_max + p.len[b]) * D + d;
+            host[0] = v0; host[1] = v1;   // the append: one write across the link
+          }
+        }
+      }
+    }
+  }
+}
+
+struct UnitRange {
+  int b, kvh, split, t_lo, t_hi, S;
+};
+
+__device__ __forceinline__ UnitRange unit_range(const DecodeParams& p, int u) {
+  UnitRange r;
+  r.split = u % p.splits;
+  const int bh = u / p.splits;
+  r.kvh = bh % p.Hkv;
+  r.b = bh / p.Hkv;
+  r.S = p.len[r.b] + 1;  // keys after the append
+  const int nt = (r.S + p.tile_n - 1) / p.tile_n;
+  r.t_lo = (int)((long long)r.split * nt / p.splits);
+  r.t_hi = (int)((long long)(r.split + 1) * nt / p.splits);
+  return r;
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int N = p.tile_n, stages = p.stages;
+  const DecodeSmem L(D, G, N, stages, p.B);
+  const int tid = threadIdx.x;
+  const int tile_bytes = N * D * 2;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + stages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flag);
+
+  if (tid == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], kProducers);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    *abort_flag = 0;
+  }
+  __syncthreads();
+
+  const int nunits = p.B * p.Hkv * p.splits;
+  constexpr int CPR = D * 2 / 16;  // 16-byte chunks per row
+
+  if (tid >= kConsumers) {
+    // ------------------------------------------------------------ producer
+    const int ptid = tid - kConsumers;
+    int it = 0;
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+      const UnitRange r = unit_range(p, u);
+      const size_t head_off = ((size_t)r.b * p.Hkv + r.kvh) * p.S_max * D;
+      const T* kg = static_cast<const T*>(p.k_read) + head_off;
+      const T* vg = static_cast<const T*>(p.v_read) + head_off;
+      const int cached = p.len[r.b];
+      for (int t = r.t_lo; t < r.t_hi; ++t, ++it) {
+        const int stage = it % stages;
+        const uint32_t par = ((it / stages) & 1) ^ 1;
+        if (!mbar_wait_bounded(&empty[stage], par, abort_flag)) {
+          if (!*abort_flag) record_timeout(p.status, kSiteEmpty);
+          *abort_flag = 1;
+          cp_async_wait_all();
+          return;
+        }
+        uint8_t* kt = smem + L.ring + stage * 2 * tile_bytes;
+        uint8_t* vt = kt + tile_bytes;
+        const int key0 = t * N;
+        const int nrows = max(0, min(N, cached - key0));  // host rows only; the new row comes from HBM
+        for (int i = ptid; i < nrows * CPR; i += kProducers) {
+          const int row = i / CPR, c = i % CPR;
+          const int dst = row * (D * 2) + swz_chunk(row, c) * 16;
+          const size_t src = (size_t)(key0 + row) * D + c * 8;
+          cp_async16(kt + dst, kg + src, 16);
+          cp_async16(vt + dst, vg + src, 16);
+        }
+        cp_async_arrive_noinc(&full[stage]);
+      }
+    }
+    cp_async_wait_all();
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int ctid = tid;
+  const int warp = ctid / 32, lane = ctid % 32;
+
+  // Phase A: projection slice of this CTA.
+  {
+    const int ncol = (p.Hq + 2 * p.Hkv) * D;
+    const int nblk = ncol / 8;
+    const int per = nblk / gridDim.x, rem = nblk % gridDim.x;
+    const int b0 = blockIdx.x * per + min((int)blockIdx.x, rem);
+    const int b1 = b0 + per + ((int)blockIdx.x < rem ? 1 : 0);
+    if (b1 > b0) project_columns<T, D>(p, b0 * 8, b1 * 8, smem, L, ctid);
+  }
+  // Grid barrier: every CTA's q and fresh k/v are in the workspace.
+  named_bar_sync(kBarConsumers, kConsumers);
+  if (ctid == 0) {
+    __threadfence();
+    atomicAdd(&p.status->grid_arrive, 1u);
+    const uint64_t deadline = global_timer_ns() + kWaitBudgetNs;
+    while (ld_acquire_gpu(&p.status->grid_arrive) < gridDim.x) {
+      if (global_timer_ns() > deadline) {
+        record_timeout(p.status, kSiteGridBarrier);
+        *abort_flag = 1;
+        break;
+      }
+    }
+  }
+  named_bar_sync(kBarConsumers, kConsumers);
+  if (*abort_flag) return;  // producers see the flag in their bounded waits
+
+  float* q_s = reinterpret_cast<float*>(smem + L.q);     // [G][D+4]
+  float* s_s = reinterpret_cast<float*>(smem + L.s);     // [2][G][N]
+  float* alpha_s = reinterpret_cast<float*>(smem + L.alpha);  // [2][G]
+  float* m_s = reinterpret_cast<float*>(smem + L.ml);    // [G]
+  float* l_s = m_s + G;                                  // [G]
+  float* red_s = reinterpret_cast<float*>(smem + L.red); // [kConsumers][2]
+
+  // score mapping
+  const int NS = N * G;
+  const int TPS = NS >= kConsumers ? 1 : kConsumers / NS;   // threads per score
+  const int SPT = NS > kConsumers ? NS / kConsumers : 1;    // scores per thread
+  const int DPT = D / TPS;                                  // dims per thread
+  // P.V mapping
+  constexpr int NP = G * D / 2;                                   // output pairs
+  constexpr int KG = NP >= kConsumers ? 1 : kConsumers / NP;      // key groups
+  constexpr int PPT = NP > kConsumers ? NP / kConsumers : 1;      // pairs per thread
+  constexpr int TPG = kConsumers / KG;                            // threads per key group
+  const int kgi = ctid / TPG;
+
+  int it = 0;
+  for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+    const UnitRange r = unit_range(p, u);
+    // q of the G heads of this KV group (bf16/fp16 values, held as fp32)
+    for (int i = ctid; i < G * D; i += kConsumers) {
+      const int g = i / D, d = i % D;
+      const T* qg = static_cast<const T*>(p.q_ws) + (size_t)r.b * p.Hq * D + (r.kvh * G + g) * D + d;
+      q_s[g * (D + 4) + d] = DT<T>::to_f(__ldcg(qg));
+    }
+    float acc[PPT][2];
+#pragma unroll
+    for (int pp = 0; pp < PPT; ++pp) acc[pp][0] = acc[pp][1] = 0.f;
+
+    for (int t = r.t_lo; t < r.t_hi; ++t, ++it) {
+      const int stage = it % stages;
+      const uint32_t par = (it / stages) & 1;
+      const int buf = it & 1;
+      const int key0 = t * N;
+      const int nvalid = min(N, r.S - key0);
+      uint8_t* kt = smem + L.ring + stage * 2 * tile_bytes;
+      uint8_t* vt = kt + tile_bytes;
+      if (ctid == 0) {
+        if (!mbar_wait_bounded(&full[stage], par, abort_flag)) {
+          if (!*abort_flag) record_timeout(p.status, kSiteFull);
+          *abort_flag = 1;
+        }
+      }
+      // the new token's row (if in this tile) comes from the HBM workspace
+      const int rnew = p.len[r.b] - key0;
+      if (rnew >= 0 && rnew < N && ctid < 2 * CPR) {
+        const int which = ctid / CPR, c = ctid % CPR;
+        const T* src = static_cast<const T*>(p.kv_ws) +
+                       ((size_t)r.b * 2 + which) * p.Hkv * D + r.kvh * D + c * 8;
+        uint8_t* dst = (which ? vt : kt) + rnew * (D * 2) + swz_chunk(rnew, c) * 16;
+        *reinterpret_cast<uint4*>(dst) = __ldcg(reinterpret_cast<const uint4*>(src));
+      }
+      named_bar_sync(kBarConsumers, kConsumers);
+      if (*abort_flag) return;
+
+      // scores s[g][n] = (q_g . k_n) * log2(e)/sqrt(D)
+      float* sb = s_s + buf * G * N;
+      for (int si = 0; si < SPT; ++si) {
+        const int sc = ctid / TPS + si * (kConsumers / TPS);
+        const int n = sc / G, g = sc % G;
+        const int part = ctid % TPS;
+        float dot = 0.f;
+        if (n < nvalid) {
+          const float* qrow = q_s + g * (D + 4) + part * DPT;
+          const uint8_t* krow = kt + n * (D * 2);
+#pragma unroll 4
+          for (int c8 = 0; c8 < DPT / 8; ++c8) {
+            const int c = part * (DPT / 8) + c8;
+            const uint4 kv = *reinterpret_cast<const uint4*>(krow + swz_chunk(n, c) * 16);
+            const float4 qa = *reinterpret_cast<const float4*>(qrow + c8 * 8);
+            const float4 qb = *reinterpret_cast<const float4*>(qrow + c8 * 8 + 4);
+            float2 k0 = DT<T>::to_f2(kv.x), k1 = DT<T>::to_f2(kv.y);
+            float2 k2 = DT<T>::to_f2(kv.z), k3 = DT<T>::to_f2(kv.w);
+            dot = fmaf(qa.x, k0.x, dot); dot = fmaf(qa.y, k0.y, dot);
+            dot = fmaf(qa.z, k1.x, dot); dot = fmaf(qa.w, k1.y, dot);
+            dot = fmaf(qb.x, k2.x, dot); dot = fmaf(qb.y, k2.y, dot);
+            dot = fmaf(qb.z, k3.x, dot); dot = fmaf(qb.w, k3.y, dot);
+          }
+        }
+        for (int off = TPS / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+        if (part == 0 && n < N) sb[g * N + n] = n < nvalid ? dot * p.scale_log2 : -INFINITY;
+      }
+      named_bar_sync(kBarConsumers, kConsumers);
+
+      // online softmax, one warp per head
+      const bool first = (t == r.t_lo);
+      if (warp < G) {
+        const int g = warp;
+        float mx = -INFINITY;
+        for (int n = lane; n < N; n += 32) mx = fmaxf(mx, sb[g * N + n]);
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float m_old = first ? -INFINITY : m_s[g];
+        const float l_old = first ? 0.f : l_s[g];
+        const float m_new = fmaxf(m_old, mx);
+        float sum = 0.f;
+        for (int n = lane; n < N; n += 32) {
+          const float e = exp2f(sb[g * N + n] - m_new);
+          sb[g * N + n] = e;
+          sum += e;
+        }
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        if (lane == 0) {
+          const float a = exp2f(m_old - m_new);
+          alpha_s[buf * G + g] = a;
+          m_s[g] = m_new;
+          l_s[g] = a * l_old + sum;
+        }
+      }
+      named_bar_sync(kBarConsumers, kConsumers);
+
+      // O = alpha * O + P . V
+#pragma unroll
+      for (int pp = 0; pp < PPT; ++pp) {
+        const int pi = ctid % TPG + pp * TPG;
+        const int g = pi / (D / 2), dp = pi % (D / 2);
+        const float a = alpha_s[buf * G + g];
+        float o0 = acc[pp][0] * a, o1 = acc[pp][1] * a;
+        const float* prow = sb + g * N;
+        const int c = dp / 4, within = (dp % 4) * 4;
+        for (int n = kgi; n < nvalid; n += KG) {
+          const float pw = prow[n];
+          const uint32_t v2 = *reinterpret_cast<const uint32_t*>(vt + n * (D * 2) +
+                                                                swz_chunk(n, c) * 16 + within);
+          const float2 v = DT<T>::to_f2(v2);
+          o0 = fmaf(pw, v.x, o0);
+          o1 = fmaf(pw, v.y, o1);
+        }
+        acc[pp][0] = o0;
+        acc[pp][1] = o1;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+
+    // unit end: fold the key groups, normalise, write the partial
+    if (KG > 1) {
+      red_s[ctid * 2] = acc[0][0];
+      red_s[ctid * 2 + 1] = acc[0][1];
+    }
+    named_bar_sync(kBarConsumers, kConsumers);
+    if (kgi == 0) {
+#pragma unroll
+      for (int pp = 0; pp < PPT; ++pp) {
+        const int pi = ctid % TPG + pp * TPG;
+        const int g = pi / (D / 2), dp = pi % (D / 2);
+        float o0 = acc[pp][0], o1 = acc[pp][1];
+        if (KG > 1) {
+          for (int k = 1; k < KG; ++k) {
+            o0 += red_s[(ctid + k * TPG) * 2];
+            o1 += red_s[(ctid + k * TPG) * 2 + 1];
+          }
+        }
+        const int h = r.kvh * G + g;
+        const size_t slot = ((size_t)r.b * p.Hq + h) * p.splits + r.split;
+        const bool empty_unit = r.t_hi <= r.t_lo;
+        const float l = empty_unit ? 1.f : l_s[g];
+        float2 o = make_float2(empty_unit ? 0.f : o0 / l, empty_unit ? 0.f : o1 / l);
+        *reinterpret_cast<float2*>(p.part_o + slot * D + dp * 2) = o;
+        if (dp == 0) p.part_lse[slot] = empty_unit ? -INFINITY : m_s[g] + log2f(l);
+      }
+    }
+    named_bar_sync(kBarConsumers, kConsumers);
+  }
+}
+
+// Split-KV combine: o = sum_i 2^(lse_i - M) o_i / sum_i 2^(lse_i - M).
+template <typename T>
+__global__ void decode_combine_kernel(const float* __restrict__ part_o,
+                                      const float* __restrict__ part_lse, T* __restrict__ out,
+                                      int splits, int D, DeviceStatus* status) {
+  const int bh = blockIdx.x;
+  const float* lse = part_lse + (size_t)bh * splits;
+  float M = -INFINITY;
+  for (int i = 0; i < splits; ++i) M = fmaxf(M, lse[i]);
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float num = 0.f, den = 0.f;
+    for (int i = 0; i < splits; ++i) {
+      const float w = exp2f(lse[i] - M);
+      num = fmaf(w, part_o[((size_t)bh * splits + i) * D + d], num);
+      den += w;
+    }
+    out[(size_t)bh * D + d] = DT<T>::from_f(num / den);
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) status->grid_arrive = 0u;
+}
+
+template <typename T, int D, int G>
+cudaError_t launch_decode_t(const DecodeParams& p, int grid, int smem, cudaStream_t s,
+                            const KernelTimer& timer) {
+  auto kern = decode_fused_kernel<T, D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  void* args[] = {const_cast<DecodeParams*>(&p)};
+  timer.before(s);
+  e = cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(kThreads), args,
+                                  (size_t)smem, s);
+  if (e != cudaSuccess) return e;
+  timer.after(s);
+  decode_combine_kernel<T><<<p.B * p.Hq, D, 0, s>>>(p.part_o, p.part_lse,
+                                                    static_cast<T*>(p.out), p.splits, D,
+                                                    p.status);
+  return cudaGetLastError();
+}
+
+template <typename T, int D, int G>
+cudaError_t occupancy_t(int smem, int* blocks) {
+  auto kern = decode_fused_kernel<T, D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, kern, kThreads, smem);
+}
+
+// Kernel repository: <dtype, head_dim, group size> instantiations.
+template <typename F>
+cudaError_t dispatch(int dtype, int D, int G, F&& f) {
+#define DKV_CASE(TT, DD, GG) \
+  if (D == DD && G == GG) return f.template operator()<TT, DD, GG>();
+  if (dtype == DKV_BF16) {
+    DKV_CASE(__nv_bfloat16, 64, 1) DKV_CASE(__nv_bfloat16, 64, 2) DKV_CASE(__nv_bfloat16, 64, 4)
+    DKV_CASE(__nv_bfloat16, 64, 8) DKV_CASE(__nv_bfloat16, 128, 1) DKV_CASE(__nv_bfloat16, 128, 2)
+    DKV_CASE(__nv_bfloat16, 128, 4) DKV_CASE(__nv_bfloat16, 128, 8)
+  } else {
+    DKV_CASE(__half, 64, 1) DKV_CASE(__half, 64, 2) DKV_CASE(__half, 64, 4)
+    DKV_CASE(__half, 64, 8) DKV_CASE(__half, 128, 1) DKV_CASE(__half, 128, 2)
+    DKV_CASE(__half, 128, 4) DKV_CASE(__half, 128, 8)
+  }
+#undef DKV_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool decode_supported(int dtype, int D, int G) {
+  return (dtype == DKV_BF16 || dtype == DKV_FP16) && (D == 64 || D == 128) &&
+         (G == 1 || G == 2 || G == 4 || G == 8);
+}
+
+int decode_smem_bytes(int dtype, int D, int G, int tile_n, int stages, int B) {
+  (void)dtype;
+  return DecodeSmem(D, G, tile_n, stages, B).total;
+}
+
+struct LaunchDecodeF {
+  const DecodeParams* p; int grid; int smem; cudaStream_t s; const KernelTimer* timer;
+  template <typename T, int D, int G> cudaError_t operator()() {
+    return launch_decode_t<T, D, G>(*p, grid, smem, s, *timer);
+  }
+};
+struct OccF {
+  int smem; int* blocks;
+  template <typename T, int D, int G> cudaError_t operator()() {
+    return occupancy_t<T, D, G>(smem, blocks);
+  }
+};
+
+cudaError_t launch_decode(const DecodeParams& p, int dtype, int grid, int smem_bytes,
+                          cudaStream_t s, int* launches, const KernelTimer& timer) {
+  LaunchDecodeF f{&p, grid, smem_bytes, s, &timer};
+  cudaError_t e = dispatch(dtype, p.D, p.Hq / p.Hkv, f);
+  if (e == cudaSuccess && launches) *launches += 2;
+  return e;
+}
+
+cudaError_t decode_occupancy(int dtype, int D, int G, int tile_n, int stages, int B,
+                             int* blocks_per_sm) {
+  OccF f{decode_smem_bytes(dtype, D, G, tile_n, stages, B), blocks_per_sm};
+  return dispatch(dtype, D, G, f);
+}
+
+}  // namespace dkv

@@ -1,0 +1,192 @@
+// Measurement kernels: the plain zero-copy streaming probe that gives the
+// host-link denominator of the roofline, a write probe, and the naive
+// untiled zero-copy attention baseline.
+//
+// The naive baseline is the pages' "naive zero-copy" ("Paper Notes:
+// DirectKV", Motivation and Experiments, CPU-aware tiling): attention pointed
+// straight at host-resident K/V, each query head re-reading its KV head's
+// rows across the link, with no shared-memory staging and no reuse.
+#include "dkv_internal.cuh"
+
+namespace dkv {
+namespace {
+
+constexpr int kProbeThreads = 256;
+
+__global__ void __launch_bounds__(kProbeThreads) probe_read_kernel(const uint4* __restrict__ src,
+                                                                   size_t n16, uint4* sink) {
+  uint32_t acc = 0;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  // four independent 16-byte loads in flight per thread per iteration
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    const uint4 a = __ldcs(src + i);
+    const uint4 b = __ldcs(src + i + stride);
+    const uint4 c = __ldcs(src + i + 2 * stride);
+    const uint4 d = __ldcs(src + i + 3 * stride);
+    acc ^= a.x ^ a.y ^ a.z ^ a.w ^ b.x ^ b.y ^ b.z ^ b.w ^ c.x ^ c.y ^ c.z ^ c.w ^ d.x ^ d.y ^
+           d.z ^ d.w;
+  }
+  for (; i < n16; i += stride) {
+    const uint4 a = __ldcs(src + i);
+    acc ^= a.x ^ a.y ^ a.z ^ a.w;
+  }
+  if (acc == 0x9E3779B9u) sink->x = acc;  // practically never; keeps the loads live
+}
+
+__global__ void __launch_bounds__(kProbeThreads) probe_write_kernel(uint4* __restrict__ dst,
+                                                                    size_t n16) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
+    __stcs(dst + i, make_uint4((uint32_t)i, 0x5A5A5A5Au, (uint32_t)(i >> 32), 0xA5A5A5A5u));
+}
+
+// Naive zero-copy attention: one CTA per (b, q head, split), 4 warps.  Each
+// lane of a warp scores its own key by reading the key row from the host
+// pointer directly; P.V reads the value rows from the host pointer directly.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) attend_naive_kernel(const T* __restrict__ q,
+                                                           const T* __restrict__ k,
+                                                           const T* __restrict__ v,
+                                                           float* part_o, float* part_lse,
+                                                           int Hq, int Hkv, int S_max,
+                                                           const LenArray lens,
+                                                           int splits, float scale_log2) {
+  __shared__ float red_o[4][D];
+  __shared__ float red_ml[4][2];
+  const int split = blockIdx.x % splits;
+  const int bh = blockIdx.x / splits;
+  const int h = bh % Hq, b = bh / Hq;
+  const int kvh = h / (Hq / Hkv);
+  const int S = lens.v[b];
+  const int lo = (int)((long long)split * S / splits), hi = (int)((long long)(split + 1) * S / splits);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  float qv[D];
+#pragma unroll
+  for (int d = 0; d < D; ++d) qv[d] = DT<T>::to_f(q[((size_t)b * Hq + h) * D + d]);
+  const T* kb = k + ((size_t)b * Hkv + kvh) * S_max * D;
+  const T* vb = v + ((size_t)b * Hkv + kvh) * S_max * D;
+  constexpr int DPL = D / 32;
+  float o[DPL];
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) o[j] = 0.f;
+  float m = -INFINITY, l = 0.f;
+  for (int base = lo + warp * 32; base < hi; base += 4 * 32) {
+    const int n = base + lane;
+    float s = -INFINITY;
+    if (n < hi) {
+      const uint4* kr = reinterpret_cast<const uint4*>(kb + (size_t)n * D);
+      float dot = 0.f;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const uint4 w = kr[c];
+        float2 a0 = DT<T>::to_f2(w.x), a1 = DT<T>::to_f2(w.y), a2 = DT<T>::to_f2(w.z),
+               a3 = DT<T>::to_f2(w.w);
+        dot += qv[c * 8 + 0] * a0.x + qv[c * 8 + 1] * a0.y + qv[c * 8 + 2] * a1.x +
+               qv[c * 8 + 3] * a1.y + qv[c * 8 + 4] * a2.x + qv[c * 8 + 5] * a2.y +
+               qv[c * 8 + 6] * a3.x + qv[c * 8 + 7] * a3.y;
+      }
+      s = dot * scale_log2;
+    }
+    float mx = s;
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float m_new = fmaxf(m, mx);
+    const float a = exp2f(m - m_new);
+    const float pw = exp2f(s - m_new);
+    float sum = pw;
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    l = l * a + sum;
+    m = m_new;
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) o[j] *= a;
+    const int cnt = min(32, hi - base);
+    for (int src = 0; src < cnt; ++src) {
+      const float pj = __shfl_sync(0xffffffffu, pw, src);
+      const T* vr = vb + (size_t)(base + src) * D;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) o[j] = fmaf(pj, DT<T>::to_f(vr[lane + 32 * j]), o[j]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) red_o[warp][lane + 32 * j] = o[j];
+  if (lane == 0) { red_ml[warp][0] = m; red_ml[warp][1] = l; }
+  __syncthreads();
+  float M = -INFINITY;
+  for (int w = 0; w < 4; ++w) M = fmaxf(M, red_ml[w][0]);
+  float L = 0.f;
+  for (int w = 0; w < 4; ++w) L += red_ml[w][1] * (red_ml[w][0] == -INFINITY ? 0.f : exp2f(red_ml[w][0] - M));
+  const size_t slot = ((size_t)b * Hq + h) * splits + split;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float acc = 0.f;
+    for (int w = 0; w < 4; ++w)
+      if (red_ml[w][0] != -INFINITY) acc += red_o[w][d] * exp2f(red_ml[w][0] - M);
+    part_o[slot * D + d] = L > 0.f ? acc / L : 0.f;
+  }
+  if (threadIdx.x == 0) part_lse[slot] = L > 0.f ? M + log2f(L) : -INFINITY;
+}
+
+template <typename T>
+__global__ void naive_combine_kernel(const float* part_o, const float* part_lse, T* out,
+                                     int splits, int D) {
+  const int bh = blockIdx.x;
+  const float* lse = part_lse + (size_t)bh * splits;
+  float M = -INFINITY;
+  for (int i = 0; i < splits; ++i) M = fmaxf(M, lse[i]);
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float num = 0.f, den = 0.f;
+    for (int i = 0; i < splits; ++i) {
+      if (lse[i] == -INFINITY) continue;
+      const float w = exp2f(lse[i] - M);
+      num = fmaf(w, part_o[((size_t)bh * splits + i) * D + d], num);
+      den += w;
+    }
+    out[(size_t)bh * D + d] = DT<T>::from_f(num / den);
+  }
+}
+
+int probe_grid() {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms * 8;
+}
+
+}  // namespace
+
+cudaError_t launch_probe_read(const void* src, size_t bytes, void* sink, cudaStream_t s) {
+  probe_read_kernel<<<probe_grid(), kProbeThreads, 0, s>>>(static_cast<const uint4*>(src),
+                                                           bytes / 16, static_cast<uint4*>(sink));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_probe_write(void* dst, size_t bytes, cudaStream_t s) {
+  probe_write_kernel<<<probe_grid(), kProbeThreads, 0, s>>>(static_cast<uint4*>(dst), bytes / 16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attend_naive(const void* q, const void* k, const void* v, void* out,
+                                float* part_o, float* part_lse, int B, int Hq, int Hkv, int D,
+                                int S_max, const int* len, int splits, int dtype,
+                                cudaStream_t s) {
+  LenArray lens;
+  for (int b = 0; b < kMaxBatch; ++b) lens.v[b] = b < B ? len[b] : 0;
+  const float sl2 = 1.4426950408889634f / sqrtf((float)D);
+  const int grid = B * Hq * splits;
+#define DKV_N(TT, DD)                                                                           \
+  {                                                                                             \
+    attend_naive_kernel<TT, DD><<<grid, 128, 0, s>>>(                                           \
+        static_cast<const TT*>(q), static_cast<const TT*>(k), static_cast<const TT*>(v), part_o, \
+        part_lse, Hq, Hkv, S_max, lens, splits, sl2);                                        \
+    naive_combine_kernel<TT><<<B * Hq, DD, 0, s>>>(part_o, part_lse, static_cast<TT*>(out),     \
+                                                   splits, DD);                                 \
+    return cudaGetLastError();                                                                  \
+  }
+  if (dtype == DKV_BF16 && D == 64) DKV_N(__nv_bfloat16, 64)
+  if (dtype == DKV_BF16 && D == 128) DKV_N(__nv_bfloat16, 128)
+  if (dtype == DKV_FP16 && D == 64) DKV_N(__half, 64)
+  if (dtype == DKV_FP16 && D == 128) DKV_N(__half, 128)
+#undef DKV_N
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dkv
