@@ -186,6 +186,38 @@ dkv_status dkv_decode_staged(dkv_cache* cache, const void* x, const void* wq, co
 dkv_status dkv_cache_kernel_timing(dkv_cache* cache, int enable);
 dkv_status dkv_cache_last_kernel_ms(dkv_cache* cache, float* ms);
 
+/* ---- decode without any allocation -------------------------------------- */
+
+/* The paper has no counterpart to this call; it exists for callers that may
+ * not allocate GPU memory at all (code running inside an allocator or
+ * memory-pool callback, plug-ins whose host runtime owns every device
+ * allocation, services that must hold a fixed memory budget after start-up).
+ *
+ * Same computation as dkv_decode on caller-owned buffers: q/k/v projection of
+ * x, append of the new k, v at row lengths[b] of k_cache / v_cache, attention
+ * over rows 0..lengths[b], result in out [B, 1, Hq, D].  k_cache and v_cache
+ * are device-accessible pointers to [batch][n_kv_heads][max_tokens][head_dim]
+ * caches (normally the mapped aliases of pinned host memory, e.g. from
+ * dkv_cache_device_ptrs); lengths is a host array [batch] that this call
+ * reads but does not advance.  All tensors are in `dtype`.
+ *
+ * It calls no cudaMalloc, cudaFree or allocating library routine.  Its
+ * scratch (8 MiB: q and fresh K/V workspace, split-KV partials, status word)
+ * is a fixed __device__ array that every GPU loading the library holds until
+ * the process exits; a shape whose scratch would exceed 8 MiB even with one
+ * key-range split is rejected with DKV_ERR_CAPACITY.  Every call on a device
+ * shares that array, so calls whose work overlaps on the GPU (other streams,
+ * other threads) race and must be serialised by the caller.  The first call
+ * on each device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture.
+ * Device-side wait timeouts are recorded in the scratch status word only.
+ * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY, CUDA, before anything is
+ * enqueued. */
+dkv_status dkv_decode_noalloc(const void* x, const void* wq, const void* wk, const void* wv,
+                              void* k_cache, void* v_cache, const int32_t* lengths, int batch,
+                              int hidden, int n_q_heads, int n_kv_heads, int head_dim,
+                              int max_tokens, dkv_dtype dtype, void* out, void* stream);
+
 /* Number of kernel launches the last dkv_decode / dkv_prefill enqueued. */
 int dkv_last_launch_count(void);
 

@@ -92,6 +92,7 @@ def lib(build_if_missing: bool = False):
         "dkv_decode_staged": [P, P, P, P, P, I, I, P, P, P, P],
         "dkv_cache_kernel_timing": [P, I],
         "dkv_cache_last_kernel_ms": [P, ctypes.POINTER(ctypes.c_float)],
+        "dkv_decode_noalloc": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -234,6 +235,16 @@ def dkv_decode_staged(h, x, wq, wk, wv, hidden, n_q_heads, out, k_stage, v_stage
     _check(lib().dkv_decode_staged(h, _ptr(x), _ptr(wq), _ptr(wk), _ptr(wv), hidden, n_q_heads,
                                    _ptr(out), _ptr(k_stage), _ptr(v_stage), _stream(stream)),
            "dkv_decode_staged")
+
+
+def dkv_decode_noalloc(x, wq, wk, wv, k_cache, v_cache, lengths, batch, hidden, n_q_heads,
+                       n_kv_heads, head_dim, max_tokens, dtype, out, stream=None):
+    """dkv_decode on caller-owned buffers with no allocation (see include/dkv.h)."""
+    lens = np.ascontiguousarray(lengths, dtype=np.int32)
+    _check(lib().dkv_decode_noalloc(_ptr(x), _ptr(wq), _ptr(wk), _ptr(wv), _ptr(k_cache),
+                                    _ptr(v_cache), lens.ctypes.data, batch, hidden, n_q_heads,
+                                    n_kv_heads, head_dim, max_tokens, _DTYPE[dtype], _ptr(out),
+                                    _stream(stream)), "dkv_decode_noalloc")
 
 
 class KVCache:

@@ -61,6 +61,11 @@ struct Workspace {
 
 }  // namespace
 
+namespace dkv {
+// Lets the other translation units report a failure through dkv_last_error().
+void set_last_error(dkv_status s, const char* msg) { fail(s, "%s", msg); }
+}  // namespace dkv
+
 struct dkv_cache {
   uint64_t magic;
   int device;
