@@ -148,6 +148,15 @@ dkv_status dkv_cache_set_tuning(dkv_cache* cache, int splits, int tile_n, int st
 const char* dkv_status_str(dkv_status s);
 const char* dkv_last_error(void);
 
+/* Projection Y[M,N] = X[M,K] . W[K,N] on the tensor cores (the Q projection
+ * step of dkv_prefill, q = x.Wq; "Paper Notes: DirectKV", Fundamental
+ * Underlying Technologies, Kernel Fusion).  Row-major device tensors in
+ * `dtype`, fp32 accumulation, one rounding to the dtype.  K must be a
+ * multiple of 8 and N of 64; rows past M and columns past N are not
+ * touched.  The caller owns all three buffers. */
+dkv_status dkv_project(const void* x, const void* w, void* y, int M, int K, int N,
+                       dkv_dtype dtype, void* stream);
+
 /* ---- measurement kernels (internal baselines and link probes) ----------- */
 
 /* Stream `bytes` (a multiple of 16) from `src` (a device pointer: a mapped

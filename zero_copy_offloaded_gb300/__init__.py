@@ -93,6 +93,7 @@ def lib(build_if_missing: bool = False):
         "dkv_cache_kernel_timing": [P, I],
         "dkv_cache_last_kernel_ms": [P, ctypes.POINTER(ctypes.c_float)],
         "dkv_decode_noalloc": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P],
+        "dkv_project": [P, P, P, I, I, I, I, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -216,6 +217,11 @@ def dkv_prefill(h, x, T, wq, wk, wv, hidden, n_q_heads, out, stream=None):
 
 def dkv_sync_status(h, stream=None):
     _check(lib().dkv_sync_status(h, _stream(stream)), "dkv_sync_status")
+
+
+def dkv_project(x, w, y, M, K, N, dtype="bf16", stream=None):
+    _check(lib().dkv_project(_ptr(x), _ptr(w), _ptr(y), M, K, N, _DTYPE[dtype], _stream(stream)),
+           "dkv_project")
 
 
 def dkv_probe_read(src, nbytes, sink, stream=None):

@@ -557,6 +557,21 @@ dkv_status dkv_sync_status(dkv_cache* c, void* stream) {
   return DKV_OK;
 }
 
+dkv_status dkv_project(const void* x, const void* w, void* y, int M, int K, int N,
+                       dkv_dtype dtype, void* stream) {
+  if (!x || !w || !y) return fail(DKV_ERR_INVALID_ARG, "null tensor pointer");
+  if (M <= 0 || K <= 0 || N <= 0 || K % 8 || N % 64)
+    return fail(DKV_ERR_INVALID_ARG, "M=%d K=%d N=%d (K must be a multiple of 8, N of 64)", M,
+                K, N);
+  if (dtype != DKV_BF16 && dtype != DKV_FP16) return fail(DKV_ERR_INVALID_ARG, "dtype");
+  cudaError_t e = launch_gemm_tc(x, w, y, M, N, K, dtype, nullptr, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "projection launch");
+  }
+  return DKV_OK;
+}
+
 dkv_status dkv_probe_read(const void* src, size_t bytes, void* sink, void* stream) {
   if (!src || !sink || bytes == 0 || bytes % 16) return fail(DKV_ERR_INVALID_ARG, "invalid argument");
   cudaError_t e = launch_probe_read(src, bytes, sink, static_cast<cudaStream_t>(stream));

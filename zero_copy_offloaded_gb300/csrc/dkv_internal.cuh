@@ -138,7 +138,7 @@ __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
 }
 
 __device__ __forceinline__ void record_timeout(DeviceStatus* st, int site) {
-  if (atomicCAS(&st->code, 0, kStatusTimeout) == 0) st->site = site;
+  if (st && atomicCAS(&st->code, 0, kStatusTimeout) == 0) st->site = site;
 }
 
 // 16-byte chunk swizzle inside a row of `row_bytes` (>= 128): chunk c of row r
@@ -219,6 +219,10 @@ bool decode_supported(int dtype, int D, int G);
 cudaError_t launch_prefill(const PrefillParams& p, int dtype, cudaStream_t s, int* launches,
                            const void* wq, const KernelTimer& timer);
 bool prefill_supported(int dtype, int D, int G);
+
+// Y[M,N] = X[M,K] . W[K,N] on the tensor cores (gemm_tc.cu).
+cudaError_t launch_gemm_tc(const void* x, const void* w, void* y, int M, int N, int K, int dtype,
+                           DeviceStatus* status, cudaStream_t s);
 
 cudaError_t launch_probe_read(const void* src, size_t bytes, void* sink, cudaStream_t s);
 cudaError_t launch_probe_write(void* dst, size_t bytes, cudaStream_t s);

@@ -108,23 +108,6 @@ struct SeqGemm {
   }
 };
 
-// Q = x . Wq for all B*T rows, rounded to T, row-major [B*T, Hq*D].
-template <typename T>
-__global__ void __launch_bounds__(kThreads) qproj_kernel(const T* __restrict__ x,
-                                                         const T* __restrict__ wq,
-                                                         T* __restrict__ q, int M, int H, int N) {
-  using G = SeqGemm<T, 256>;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int r0 = blockIdx.y * G::kRows;
-  const int c0 = blockIdx.x * 256;
-  const int nrows = min(G::kRows, M - r0);
-  auto bptr = [&](int j, int c) { return wq + (size_t)j * N + c0 + c; };
-  auto epi = [&](int r, int c, float v) {
-    q[(size_t)(r0 + r) * N + c0 + c] = DT<T>::from_f(v);
-  };
-  G::run(x + (size_t)r0 * H, H, nrows, bptr, smem, epi, min(256, N - c0));
-}
-
 // ---------------------------------------------------------------------------
 template <int D>
 struct PrefillCfg {
@@ -314,19 +297,11 @@ __global__ void prefill_combine_kernel(const PrefillParams p, int C) {
 template <typename T, int D, int G>
 cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t s, int* launches,
                              const void* wq, const KernelTimer& timer) {
-  // 1. Q projection (HBM-resident Q)
+  // 1. Q projection (HBM-resident Q) on the tensor cores
   {
-    using Q = SeqGemm<T, 256>;
-    auto kern = qproj_kernel<T>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Q::kSmemBytes);
+    cudaError_t e = launch_gemm_tc(p.x, wq, const_cast<void*>(p.q), p.B * p.T, p.Hq * D, p.H,
+                                   DT<T>::code, p.status, s);
     if (e != cudaSuccess) return e;
-    const int M = p.B * p.T, N = p.Hq * D;
-    dim3 grid((N + 255) / 256, (M + Q::kRows - 1) / Q::kRows);
-    kern<<<grid, kThreads, Q::kSmemBytes, s>>>(static_cast<const T*>(p.x),
-                                               static_cast<const T*>(wq),
-                                               static_cast<T*>(const_cast<void*>(p.q)), M, p.H, N);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   // 2. fused KV projection + append + KV-stationary attention
   {
