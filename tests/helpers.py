@@ -33,6 +33,33 @@ def out_f64(t, dtype) -> np.ndarray:
     return oracle.decode_bits(to_bits(t), dtype)
 
 
+def ulp_distance(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Distance in representable steps between two arrays of 16-bit float bits."""
+    def ordered(x):
+        x = x.astype(np.int32)
+        return np.where(x & 0x8000, -(x & 0x7FFF), x)
+    return np.abs(ordered(a) - ordered(b))
+
+
+def assert_projection_close(got_bits, x_bits, w_bits, dtype, what=""):
+    """A tensor-core projection against the oracle's fp32-sequential one.
+
+    got_bits [rows, N], x_bits [rows, K], w_bits [K, N].  Each element is
+    within 1 ulp of the oracle's, or (where the sum nearly cancels) within the
+    fp32 summation error bound K * 2^-24 * sum|x_j w_j| plus half an ulp of
+    the exact sum.  Returns (bit-exact fraction, within-1-ulp fraction)."""
+    import oracle
+    ref, exact = oracle.project(x_bits, w_bits, dtype, exact=True)
+    xf, wf = oracle.decode_bits(x_bits, dtype), oracle.decode_bits(w_bits, dtype)
+    bound = x_bits.shape[1] * 2.0 ** -24 * (np.abs(xf) @ np.abs(wf))
+    d = ulp_distance(got_bits, ref)
+    g = oracle.decode_bits(got_bits, dtype)
+    half_ulp = np.abs(g) * (2.0 ** -8 if dtype == "bf16" else 2.0 ** -11) + 1e-30
+    ok = (d <= 1) | (np.abs(g - exact) <= bound + half_ulp)
+    assert ok.all(), f"{what}: {(~ok).sum()} elements beyond 1 ulp and the fp32 error bound"
+    return float(np.mean(d == 0)), float(np.mean(d <= 1))
+
+
 def errors(got: np.ndarray, ref: np.ndarray):
     d = np.abs(got - ref)
     return float(d.max()), float(d.sum() / max(np.abs(ref).sum(), 1e-300))

@@ -1,17 +1,18 @@
 """Prefill parity: Q projection + fused KV-stationary prefill + combine
 (through the C ABI) against the fp64 oracle on the same seeded inputs.
 
-Bars as for decode: appended K/V rows equal the oracle's fp32-sequential
-projection rounded to the dtype (bit-exact while the projection is an fp32
-chain over H in order); attention output max-abs <= 1e-2 and
-sum|err|/sum|ref| <= 2e-3 versus fp64; prefix rows and rows past the
-append untouched."""
+Bars: appended K/V rows within 1 ulp of the oracle's fp32-sequential
+projection rounded to the dtype (the fused projection runs on the tensor
+cores, whose summation order differs), or within the fp32 summation error
+bound where the sum nearly cancels; attention output max-abs <= 1e-2 and
+sum|err|/sum|ref| <= 2e-3 versus fp64; prefix rows and rows past the append
+untouched."""
 import numpy as np
 import pytest
 
 from zero_copy_offloaded_gb300 import workloads as wl
 
-from .helpers import Case, assert_close, out_f64
+from .helpers import Case, assert_close, assert_projection_close, out_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -27,10 +28,12 @@ def check_prefill(case: Case, out, ref, label="", rows=None):
         r = np.stack([ref["out"][(b, t)] for (b, t) in rows])
         res = assert_close(g, r, label)
     kh, vh = case.cache.k_host, case.cache.v_host
+    x = case.dense["x"]
     for b in range(w.B):
         p = int(case.lens[b])
-        assert np.array_equal(kh[b, :, p:p + T], ref["k_new"][b].transpose(1, 0, 2)), f"{label} k"
-        assert np.array_equal(vh[b, :, p:p + T], ref["v_new"][b].transpose(1, 0, 2)), f"{label} v"
+        for name, host, wmat in (("k", kh, case.dense["wk"]), ("v", vh, case.dense["wv"])):
+            got = host[b, :, p:p + T].transpose(1, 0, 2).reshape(T, w.Hkv * w.D)
+            assert_projection_close(got, x[b], wmat, w.dtype, f"{label} {name} append b={b}")
         assert np.array_equal(kh[b, :, :p], case.k0[b, :, :p])
         assert np.array_equal(vh[b, :, :p], case.v0[b, :, :p])
         assert np.all(kh[b, :, p + T:] == 0x7E57) and np.all(vh[b, :, p + T:] == 0x7E57)

@@ -420,11 +420,11 @@ dkv_status dkv_cache_reserve(dkv_cache* c, int n_q_heads, int max_new_tokens) {
     need = align_up((size_t)B * Hq * D * 2, 256) + align_up((size_t)B * 2 * c->Hkv * D * 2, 256) +
            align_up((size_t)B * Hq * splits * D * 4, 256) + align_up((size_t)B * Hq * splits * 4, 256);
   }
-  const int C = prefill_chunk_keys(D);
+  const int C = prefill_tc_chunk_keys();
   const size_t nch = (size_t)(c->max_tokens + C - 1) / C;
   const size_t rows = (size_t)B * T * Hq;
-  const size_t pre = align_up(rows * D * 2, 256) + align_up(nch * rows * D * 4, 256) +
-                     align_up(nch * rows * 4, 256);
+  const size_t pre = align_up(rows * D * 2, 256) + align_up(nch * rows * D * 2, 256) +
+                     align_up(nch * rows * 4, 256) + align_up(nch * B * c->Hkv * 4, 256);
   return ensure_ws(c, std::max(need, pre));
 }
 
@@ -474,15 +474,16 @@ dkv_status dkv_prefill(dkv_cache* c, const void* x, int T, const void* wq, const
   if (!prefill_supported(c->dtype, c->D, G))
     return fail(DKV_ERR_UNSUPPORTED, "no prefill kernel for dtype=%d D=%d G=%d", c->dtype, c->D, G);
   const int B = c->B, D = c->D, Hq = n_q_heads;
-  const int C = prefill_chunk_keys(D);
+  const int C = prefill_tc_chunk_keys();
   int maxS = 0;
   for (int b = 0; b < B; ++b) maxS = std::max(maxS, c->len[b] + T);
   const int nchunks = (maxS + C - 1) / C;
   const size_t rows = (size_t)B * T * Hq;
   const size_t q_b = align_up(rows * D * 2, 256);
-  const size_t po_b = align_up((size_t)nchunks * rows * D * 4, 256);
+  const size_t po_b = align_up((size_t)nchunks * rows * D * 2, 256);  // partials in the dtype
   const size_t pl_b = align_up((size_t)nchunks * rows * 4, 256);
-  if ((st = ensure_ws(c, q_b + po_b + pl_b)) != DKV_OK) return st;
+  const size_t pk_b = align_up((size_t)nchunks * B * c->Hkv * 4, 256);
+  if ((st = ensure_ws(c, q_b + po_b + pl_b + pk_b)) != DKV_OK) return st;
   char* w = static_cast<char*>(c->ws.base);
   PrefillParams p;
   memset(&p, 0, sizeof p);
@@ -490,6 +491,7 @@ dkv_status dkv_prefill(dkv_cache* c, const void* x, int T, const void* wq, const
   p.k_read = c->k_dev; p.v_read = c->v_dev; p.k_host = c->k_dev; p.v_host = c->v_dev;
   p.part_o = w + q_b;
   p.part_lse = reinterpret_cast<float*>(w + q_b + po_b);
+  p.part_k = reinterpret_cast<int*>(w + q_b + po_b + pl_b);
   p.status = c->status;
   p.out = out;
   p.B = B; p.T = T; p.H = hidden; p.Hq = Hq; p.Hkv = c->Hkv; p.D = D; p.S_max = c->max_tokens;
@@ -498,7 +500,7 @@ dkv_status dkv_prefill(dkv_cache* c, const void* x, int T, const void* wq, const
   fill_lens(p.len, c->len);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   g_last_launches = 0;
-  cudaError_t e = launch_prefill(p, c->dtype, s, &g_last_launches, wq, c->timer);
+  cudaError_t e = launch_prefill_tc(p, c->dtype, wq, s, &g_last_launches, c->timer);
   c->timer_used = c->timer.start != nullptr;
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -191,6 +191,7 @@ struct PrefillParams {
   void* v_host;
   void* part_o;      // [nchunks, B*T*Hq, D] dtype (normalised per chunk)
   float* part_lse;   // [nchunks, B*T*Hq]  (log2 domain)
+  int* part_k;       // [nchunks, B*Hkv]: partials of a chunk are stored times 2^-k
   DeviceStatus* status;
   void* out;         // [B, T, Hq, D]
   int B, T, H, Hq, Hkv, D, S_max;
@@ -219,6 +220,12 @@ bool decode_supported(int dtype, int D, int G);
 cudaError_t launch_prefill(const PrefillParams& p, int dtype, cudaStream_t s, int* launches,
                            const void* wq, const KernelTimer& timer);
 bool prefill_supported(int dtype, int D, int G);
+
+// Tensor-core prefill (prefill_tc.cu): Q projection, fused KV-stationary
+// attention with bf16/fp16 partials, combine.  Keys per stationary chunk:
+int prefill_tc_chunk_keys();
+cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, const void* wq, cudaStream_t s,
+                              int* launches, const KernelTimer& timer);
 
 // Y[M,N] = X[M,K] . W[K,N] on the tensor cores (gemm_tc.cu).
 cudaError_t launch_gemm_tc(const void* x, const void* w, void* y, int M, int N, int K, int dtype,

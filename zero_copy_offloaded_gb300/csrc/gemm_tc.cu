@@ -175,6 +175,23 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, int dtype, uint64_t rows, 
   return r == CUDA_SUCCESS;
 }
 
+// Q as [tokens][Hq][D] (row-major [tokens, Hq*D]); box = 64 of D x G heads x
+// TQ tokens, so a box lands as G*TQ rows of 128 bytes, ordered (token, head).
+bool make_tmap_q(CUtensorMap* map, const void* q, int dtype, int D, int Hq, uint64_t tokens,
+                 int G, int TQ) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, tokens};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)TQ};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, dtype == DKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  3, const_cast<void*>(q), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 cudaError_t launch_gemm_tc(const void* x, const void* w, void* y, int M, int N, int K, int dtype,
                            DeviceStatus* status, cudaStream_t s) {
   if (M <= 0 || N <= 0 || K <= 0 || N % 64 != 0 || K % 8 != 0) return cudaErrorInvalidValue;
