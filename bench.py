@@ -196,6 +196,21 @@ def main():
 
     pk = peaks()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    if args.prefill_only:
+        # prefill alone (profiling aid): link/HBM rates from the probes, then the prefill
+        probe_cache = dkv.KVCache(1, 8, 128, 65536, "bf16")
+        kd, _ = dkv.dkv_cache_device_ptrs(probe_cache.h)
+        sink = torch.zeros(4, dtype=torch.int32, device=dev)
+        nbytes = 8 * 65536 * 128 * 2
+        best = min(_time_once(torch, stream, flush,
+                              lambda: dkv.dkv_probe_read(kd, nbytes, sink, stream)) for _ in range(3))
+        link_rd = nbytes / (best * 1e-3) / 1e9
+        probe_cache.free()
+        res = bench_prefill(args, dkv, torch, dev, stream, flush, pk, link_rd, link_rd * 0.9,
+                            pk.get("hbm_gbs") or 6800.0)
+        if rank == 0:
+            print(json.dumps({"prefill": res, "link_read_gbs": link_rd}), flush=True)
+        return
     w = wl.WORKLOADS[args.workload]
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
 
@@ -364,6 +379,16 @@ def main():
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def _time_once(torch, stream, flush, fn):
+    flush.zero_()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    fn()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b)
 
 
 def bench_prefill(args, dkv, torch, dev, stream, flush, pk, link_rd, link_wr, hbm_rd):

@@ -15,8 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libdkv.so")
-SOURCES = ["dkv_api.cu", "decode.cu", "prefill.cu", "probes.cu", "decode_noalloc.cu",
-           "gemm_tc.cu", "prefill_tc.cu"]
+SOURCES = ["dkv_api.cu", "decode.cu", "probes.cu", "decode_noalloc.cu", "gemm_tc.cu",
+           "prefill_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -27,10 +27,6 @@
 
 using namespace dkv;
 
-namespace dkv {
-int prefill_chunk_keys(int D);
-}
-
 namespace {
 
 constexpr uint64_t kMagic = 0x444B5643414348ull;  // "DKVCACH"

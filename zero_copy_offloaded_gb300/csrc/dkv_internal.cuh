@@ -217,12 +217,9 @@ cudaError_t decode_occupancy(int dtype, int D, int G, int tile_n, int stages, in
                              int* blocks_per_sm);
 bool decode_supported(int dtype, int D, int G);
 
-cudaError_t launch_prefill(const PrefillParams& p, int dtype, cudaStream_t s, int* launches,
-                           const void* wq, const KernelTimer& timer);
-bool prefill_supported(int dtype, int D, int G);
-
 // Tensor-core prefill (prefill_tc.cu): Q projection, fused KV-stationary
-// attention with bf16/fp16 partials, combine.  Keys per stationary chunk:
+// attention with fp16 partials, combine.  Keys per stationary chunk:
+bool prefill_supported(int dtype, int D, int G);
 int prefill_tc_chunk_keys();
 cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, const void* wq, cudaStream_t s,
                               int* launches, const KernelTimer& timer);

@@ -192,6 +192,20 @@ bool make_tmap_q(CUtensorMap* map, const void* q, int dtype, int D, int Hq, uint
   return r == CUDA_SUCCESS;
 }
 
+// fp16 partials [blocks][rows][D]: box = 64 of D x 128 rows x 1 block.
+bool make_tmap_partial(CUtensorMap* map, void* base, int D, uint64_t rows, uint64_t blocks) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, rows, blocks};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, rows * D * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 cudaError_t launch_gemm_tc(const void* x, const void* w, void* y, int M, int N, int K, int dtype,
                            DeviceStatus* status, cudaStream_t s) {
   if (M <= 0 || N <= 0 || K <= 0 || N % 64 != 0 || K % 8 != 0) return cudaErrorInvalidValue;

@@ -17,18 +17,17 @@
 //   2. Every Q tile of the KV group that can see the chunk (128 rows = 128/G
 //      tokens x G heads, TMA from HBM) runs S = Q.K^T (tcgen05, TMEM), a
 //      complete softmax over the chunk (it is stationary, so there is no
-//      running rescale), O = P.V (tcgen05, TMEM), and its normalised O and
-//      base-2 log-sum-exp are written as the chunk's partial.  S, O, P and the
-//      Q tile are double-buffered so the tensor cores work on tile i+1 while
-//      the softmax warps finish tile i.
+//      running rescale), O = P.V (tcgen05, TMEM, fp16 operands), and its
+//      normalised O and base-2 log-sum-exp are written as the chunk's
+//      partial.  Two softmax warpgroups take alternate Q tiles, each with its
+//      own S and O in TMEM and its own P tile in shared memory, so the tensor
+//      cores run one group's MMAs while the other group does its softmax.
 // A combine kernel merges the chunks' partials per query row.
 //
-// Warp roles (192 threads): warp 0 loads (TMA / cp.async), warp 1 allocates
-// TMEM and issues every MMA from one thread, warps 2-5 run the projection
-// epilogue, the softmax and the output epilogue (one TMEM lane = one row per
-// thread).  Every wait is bounded.
-#include <mutex>
-
+// Warp roles (320 threads): warp 0 loads (TMA / cp.async), warp 1 allocates
+// TMEM and issues every MMA from one thread, warps 2-5 and 6-9 are the two
+// softmax / epilogue groups (one TMEM lane = one row per thread).  Every wait
+// is bounded.
 #include "tc_common.cuh"
 
 namespace dkv {
@@ -37,12 +36,13 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, int dtype, uint64_t rows, 
                   uint32_t box_cols, uint32_t box_rows);
 bool make_tmap_q(CUtensorMap* map, const void* q, int dtype, int D, int Hq, uint64_t tokens,
                  int G, int TQ);
+bool make_tmap_partial(CUtensorMap* map, void* base, int D, uint64_t rows, uint64_t blocks);
 
 namespace {
 
 constexpr int kC = 128;        // keys per stationary chunk
 constexpr int kBQ = 128;       // rows per Q tile
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kThreads = 320;  // 10 warps
 constexpr int kRegion = 128 * 128;  // one 128-row x 128-byte swizzled region
 
 template <int D>
@@ -95,12 +95,33 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
   return false;
 }
 
+// Warp-uniform bounded wait (tcgen05.ld after it needs the whole warp).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Bars* bars,
+                                          DeviceStatus* st, int site) {
+  return __all_sync(0xffffffffu, wait_or_abort(bar, parity, bars, st, site));
+}
+
+__device__ __forceinline__ int swz_off(int row, int cc) {  // 16-byte chunk cc of a row
+  return (cc / 8) * kRegion + row * 128 + (((cc % 8) ^ (row % 8)) * 16);
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 pack8(const uint32_t* r, float mul) {
+  uint4 o;
+  o.x = tc::pack2<T>(__uint_as_float(r[0]) * mul, __uint_as_float(r[1]) * mul);
+  o.y = tc::pack2<T>(__uint_as_float(r[2]) * mul, __uint_as_float(r[3]) * mul);
+  o.z = tc::pack2<T>(__uint_as_float(r[4]) * mul, __uint_as_float(r[5]) * mul);
+  o.w = tc::pack2<T>(__uint_as_float(r[6]) * mul, __uint_as_float(r[7]) * mul);
+  return o;
+}
+
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_x,
                       const __grid_constant__ CUtensorMap map_wk,
-                      const __grid_constant__ CUtensorMap map_wv, const TcArgs a) {
+                      const __grid_constant__ CUtensorMap map_wv,
+                      const __grid_constant__ CUtensorMap map_po, const TcArgs a) {
   using Cfg = TcCfg<D>;
   constexpr int DR = Cfg::DR;
   constexpr int TQ = kBQ / G;  // tokens per Q tile
@@ -141,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->pr_empty[i], 1);
     }
     mbar_init(&bars->kv_host, 32);
-    mbar_init(&bars->kv_ready, 4);
+    mbar_init(&bars->kv_ready, 8);
     mbar_init(&bars->pr_done, 1);
     bars->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -153,8 +174,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   // TMEM columns: S[0] 0..127, S[1] 128..255, O[0] 256.., O[1] 384..; the
   // projection accumulator (2D columns) reuses 0..2D-1 before the Q loop.
-  const uint32_t tm_s[2] = {tmem, tmem + 128};
-  const uint32_t tm_o[2] = {tmem + 256, tmem + 384};
   const int nk_proj = (a.H + 63) / 64;  // TMA zero-fills past H
   const size_t head_off = ((size_t)b * a.Hkv + kvh) * a.S_max * D;
 
@@ -168,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rows = has_new ? nhost : kC;  // zero-fill the tail when nothing is projected
       for (int i = lane; i < rows * CPR; i += 32) {
         const int r = i / CPR, cc = i % CPR;
-        const int off = (cc / 8) * kRegion + r * 128 + (((cc % 8) ^ (r % 8)) * 16);
+        const int off = swz_off(r, cc);
         const bool ok = r < nhost;
         const size_t src = ok ? (size_t)r * D + cc * 8 : 0;
         cp_async16(ks + off, kg + src, ok ? 16 : 0);
@@ -250,9 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           return;
         tc::fence_after_sync();
         const uint32_t pa = smem_u32(ps + s * Cfg::kP);
+        const uint32_t o_tm = tmem + 256 + s * 128;
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
-          tc::mma_ss(tm_o[s], tc::sdesc_sw128(pa + (kk / 4) * kRegion + (kk % 4) * 32, 16, 1024),
+          tc::mma_ss(o_tm, tc::sdesc_sw128(pa + (kk / 4) * kRegion + (kk % 4) * 32, 16, 1024),
                      tc::sdesc_sw128(va + kk * 2048, kRegion, 1024), idesc_o, kk != 0);
         tc::mma_commit(&bars->o_full[s]);
         tc::mma_commit(&bars->p_empty[s]);
@@ -264,9 +284,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         tc::fence_after_sync();
         const uint32_t qa = smem_u32(qs + s * Cfg::kQ);
+        const uint32_t s_tm = tmem + s * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma_ss(tm_s[s], tc::sdesc_sw128(qa + (kk / 4) * kRegion + (kk % 4) * 32, 16, 1024),
+          tc::mma_ss(s_tm, tc::sdesc_sw128(qa + (kk / 4) * kRegion + (kk % 4) * 32, 16, 1024),
                      tc::sdesc_sw128(ka + (kk / 4) * kRegion + (kk % 4) * 32, 16, 1024), idesc_s,
                      kk != 0);
         tc::mma_commit(&bars->s_full[s]);
@@ -277,61 +298,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ==================================================== softmax / epilogue
+    // ============================================ two softmax / epilogue groups
+    const int grp = (warp - 2) / 4;           // group g takes tiles i with i % 2 == g
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;      // tile row = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    // (a) projection epilogue: round, write into the stationary tile, append
+
+    // (a) projection epilogue: group 0 takes the K columns, group 1 the V
+    //     columns; round, write into the stationary tile, append to the host.
     if (has_new) {
-      const bool ok = __all_sync(0xffffffffu,
-                                 wait_or_abort(&bars->pr_done, 0, bars, a.status, kSiteFull));
+      const bool ok = warp_wait(&bars->pr_done, 0, bars, a.status, kSiteFull);
       tc::fence_after_sync();
-      const int key = k0 + row;
-      if (ok) {  // warp-uniform: every lane runs the TMEM loads
-        const bool mine = row >= P - k0;  // this row is a new key projected here
-        T* kh = static_cast<T*>(a.k_host) + head_off + (size_t)key * D;
-        T* vh = static_cast<T*>(a.v_host) + head_off + (size_t)key * D;
+      if (ok) {
+        const int key = k0 + row;
+        const bool mine = row >= P - k0;      // this row is a new key projected here
         const bool append = mine && key < S;
+        uint8_t* tile = grp ? vs : ks;
+        T* host = static_cast<T*>(grp ? a.v_host : a.k_host) + head_off + (size_t)key * D;
 #pragma unroll 1
-        for (int part = 0; part < 2 * D / 32; ++part) {  // K columns, then V columns
+        for (int part = 0; part < D / 32; ++part) {
           uint32_t r[32];
-          tc::tmem_ld32(tmem + lane_off + part * 32, r);
+          tc::tmem_ld32(tmem + lane_off + grp * D + part * 32, r);
           tc::tmem_wait_ld();
-          const bool isv = part >= D / 32;
-          const int d0 = (part % (D / 32)) * 32;
-          uint8_t* tile = isv ? vs : ks;
-          T* host = isv ? vh : kh;
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            uint4 o;
-            o.x = tc::pack2<T>(__uint_as_float(r[v * 8 + 0]), __uint_as_float(r[v * 8 + 1]));
-            o.y = tc::pack2<T>(__uint_as_float(r[v * 8 + 2]), __uint_as_float(r[v * 8 + 3]));
-            o.z = tc::pack2<T>(__uint_as_float(r[v * 8 + 4]), __uint_as_float(r[v * 8 + 5]));
-            o.w = tc::pack2<T>(__uint_as_float(r[v * 8 + 6]), __uint_as_float(r[v * 8 + 7]));
-            const int cc = (d0 + v * 8) / 8;  // 16-byte chunk index in the row
-            if (mine)
-              *reinterpret_cast<uint4*>(tile + (cc / 8) * kRegion + row * 128 +
-                                        (((cc % 8) ^ (row % 8)) * 16)) = o;
-            if (append) *reinterpret_cast<uint4*>(host + d0 + v * 8) = o;  // the append
+            const uint4 o = pack8<T>(r + v * 8, 1.f);
+            if (mine) *reinterpret_cast<uint4*>(tile + swz_off(row, part * 4 + v)) = o;
+            if (append) *reinterpret_cast<uint4*>(host + part * 32 + v * 8) = o;  // the append
           }
         }
       }
     }
     // the host rows have landed (loader's cp.async tracked by kv_host)
     wait_or_abort(&bars->kv_host, 0, bars, a.status, kSiteFull);
-    // P.V runs in fp16 (P keeps 11 significant bits).  For bf16 inputs the
-    // stationary V chunk is converted to fp16 in place, times 2^-k with k the
-    // smallest power making max|V| < 2^15 (k = 0 unless V is huge); the
-    // chunk's partials carry that factor and the combine undoes it exactly.
-    {
+    if (grp == 1) {
+      // P.V runs in fp16 (P keeps 11 significant bits).  For bf16 inputs the
+      // stationary V chunk is converted to fp16 in place, times 2^-k with k the
+      // smallest power making max|V| < 2^15 (k = 0 unless V is huge); the
+      // chunk's partials carry that factor and the combine undoes it exactly.
       int k = 0;
       if constexpr (DT<T>::code == DKV_BF16) {
-        uint8_t* vrow = vs;  // this thread's row: key `row`
         float vmax = 0.f;
 #pragma unroll
         for (int cc = 0; cc < D / 8; ++cc) {
-          const uint4 u = *reinterpret_cast<const uint4*>(
-              vrow + (cc / 8) * kRegion + row * 128 + (((cc % 8) ^ (row % 8)) * 16));
+          const uint4 u = *reinterpret_cast<const uint4*>(vs + swz_off(row, cc));
           const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -342,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int off = 16; off > 0; off >>= 1)
           vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
         if (lane == 0) bars->vmax[quarter] = vmax;
-        named_bar_sync(1, 128);
+        named_bar_sync(2, 128);
         vmax = fmaxf(fmaxf(bars->vmax[0], bars->vmax[1]), fmaxf(bars->vmax[2], bars->vmax[3]));
         int e2 = 0;
         (void)frexpf(vmax, &e2);  // vmax < 2^e2
@@ -350,8 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sc = exp2f((float)-k);
 #pragma unroll
         for (int cc = 0; cc < D / 8; ++cc) {
-          uint4* p16 = reinterpret_cast<uint4*>(vrow + (cc / 8) * kRegion + row * 128 +
-                                                 (((cc % 8) ^ (row % 8)) * 16));
+          uint4* p16 = reinterpret_cast<uint4*>(vs + swz_off(row, cc));
           const uint4 u = *p16;
           const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
           uint32_t h4[4];
@@ -363,110 +372,116 @@ __global__ void __launch_bounds__(kThreads, 1)
           *p16 = make_uint4(h4[0], h4[1], h4[2], h4[3]);
         }
       }
-      if (threadIdx.x == 64) a.part_k[(size_t)c * a.B * a.Hkv + bh] = k;
+      if (warp == 6 && lane == 0) a.part_k[(size_t)c * a.B * a.Hkv + bh] = k;
     }
     tc::fence_proxy_async_smem();  // generic/cp.async smem writes -> tensor core reads
     tc::fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars->kv_ready);
 
-    // (b) Q tiles: softmax of tile i, then the output epilogue of tile i-1
-    float m_prev = 0.f, l_prev = 1.f;
-    int t_prev = 0;
+    // (b) this group's Q tiles: softmax, then the output epilogue
     const float scale = a.scale_log2;
-    auto epilogue = [&](int j, float m, float l, bool live) {
-      const int s = j & 1;
-      const bool ok = __all_sync(0xffffffffu, wait_or_abort(&bars->o_full[s], (j >> 1) & 1, bars,
-                                                            a.status, kSiteFull));
+    const int s = grp;
+    const uint32_t s_tm = tmem + s * 128 + lane_off;
+    const uint32_t o_tm = tmem + 256 + s * 128 + lane_off;
+    uint8_t* prow = ps + s * Cfg::kP;
+    const bool leader = warp == 2 + 4 * grp && lane == 0;  // issues this group's TMA stores
+    // partials of this unit: block (c, b, kvh) of T*G rows ordered (token, head)
+    const size_t TG = (size_t)a.T * G;
+    const size_t blk = ((size_t)c * a.B + b) * a.Hkv + kvh;
+    for (int i = grp; i < ntiles; i += 2) {
+      const uint32_t ph = (i >> 1) & 1;
+      if (!warp_wait(&bars->s_full[s], ph, bars, a.status, kSiteFull)) break;
       tc::fence_after_sync();
-      if (!ok) return;
-      const int t = t_lo + j * TQ + row / G;
-      const int h = kvh * G + row % G;
-      const size_t grow = ((size_t)b * a.T + t) * a.Hq + h;
-      const size_t slot = (size_t)c * ((size_t)a.B * a.T * a.Hq) + grow;
-      const float inv = 1.f / l;
-      __half* po = static_cast<__half*>(a.part_o) + slot * D;
-#pragma unroll 1
-      for (int part = 0; part < D / 32; ++part) {
-        uint32_t r[32];
-        tc::tmem_ld32(tm_o[s] + lane_off + part * 32, r);
-        tc::tmem_wait_ld();
-        if (live && t < a.T) {
+      const int t_first = t_lo + i * TQ;
+      // every key of the chunk is visible to every row of this tile
+      const bool full = nkeys == kC && P + t_first >= k0 + kC - 1;
+      const int t = t_first + row / G;
+      const int nvis = min(nkeys, P + t - k0 + 1);
+      // the whole S row in registers: four TMEM loads in flight, one wait
+      uint32_t r[kC];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 o;
-            o.x = tc::pack2<__half>(__uint_as_float(r[v * 8 + 0]) * inv, __uint_as_float(r[v * 8 + 1]) * inv);
-            o.y = tc::pack2<__half>(__uint_as_float(r[v * 8 + 2]) * inv, __uint_as_float(r[v * 8 + 3]) * inv);
-            o.z = tc::pack2<__half>(__uint_as_float(r[v * 8 + 4]) * inv, __uint_as_float(r[v * 8 + 5]) * inv);
-            o.w = tc::pack2<__half>(__uint_as_float(r[v * 8 + 6]) * inv, __uint_as_float(r[v * 8 + 7]) * inv);
-            *reinterpret_cast<uint4*>(po + part * 32 + v * 8) = o;
-          }
-        }
-      }
-      if (live && t < a.T) a.part_lse[slot] = m + log2f(l);
+      for (int part = 0; part < kC / 32; ++part)
+        tc::tmem_ld32(s_tm + part * 32, *reinterpret_cast<uint32_t(*)[32]>(r + part * 32));
+      tc::tmem_wait_ld();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->o_empty[s]);
-    };
-
-    for (int i = 0; i < ntiles; ++i) {
-      const int s = i & 1;
-      const bool ok = __all_sync(0xffffffffu, wait_or_abort(&bars->s_full[s], (i >> 1) & 1, bars,
-                                                            a.status, kSiteFull));
-      tc::fence_after_sync();
-      if (!ok) break;
-      const int t = t_lo + i * TQ + row / G;
-      const int qpos = P + t;
-      const int nvis = min(nkeys, qpos - k0 + 1);  // keys 0..nvis-1 visible to this row
-      float sv[kC];
+      if (lane == 0) mbar_arrive(&bars->s_empty[s]);  // S may be overwritten by tile i + 2
+      // row max of the visible raw scores (eight independent chains)
+      float m8[8];
 #pragma unroll
-      for (int part = 0; part < kC / 32; ++part) {
-        uint32_t r[32];
-        tc::tmem_ld32(tm_s[s] + lane_off + part * 32, r);
-        tc::tmem_wait_ld();
+      for (int q = 0; q < 8; ++q) m8[q] = -INFINITY;
+      if (full) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sv[part * 32 + j] = __uint_as_float(r[j]);
+        for (int j = 0; j < kC; ++j) m8[j % 8] = fmaxf(m8[j % 8], __uint_as_float(r[j]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < kC; ++j)
+          if (j < nvis) m8[j % 8] = fmaxf(m8[j % 8], __uint_as_float(r[j]));
       }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_empty[s]);  // S buffer may be overwritten
-      float mx = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < kC; ++j) {
-        sv[j] = j < nvis ? sv[j] * scale : -INFINITY;
-        mx = fmaxf(mx, sv[j]);
+      const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      const float mx = mraw * scale;
+      // P = 2^(s*scale - m) in fp16; l sums the rounded weights so the P.V
+      // product is normalised by exactly the weights it used.
+      if (!warp_wait(&bars->p_empty[s], ph ^ 1, bars, a.status, kSiteEmpty)) break;
+      // the P buffer also staged the previous tile's output: its TMA store
+      // must have finished reading it
+      if (i >= 2) {
+        if (leader) tc::bulk_wait_read_all();
+        named_bar_sync(3 + grp, 128);
       }
-      // P = 2^(s - m) rounded to the dtype; l sums the rounded values so the
-      // P.V product is normalised by exactly the weights it used.
-      if (!__all_sync(0xffffffffu, wait_or_abort(&bars->p_empty[s], ((i >> 1) & 1) ^ 1, bars,
-                                                 a.status, kSiteEmpty)))
-        break;
-      uint8_t* prow = ps + s * Cfg::kP;
-      float l = 0.f;
+      float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int cc = 0; cc < kC / 8; ++cc) {  // 16-byte chunks of the P row
+      for (int cc = 0; cc < kC / 8; ++cc) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float p0 = exp2f(sv[cc * 8 + 2 * e] - mx);
-          const float p1 = exp2f(sv[cc * 8 + 2 * e + 1] - mx);
+          const int j = cc * 8 + 2 * e;
+          float p0 = tc::ex2_approx(fmaf(__uint_as_float(r[j]), scale, -mx));
+          float p1 = tc::ex2_approx(fmaf(__uint_as_float(r[j + 1]), scale, -mx));
+          if (!full) {
+            p0 = j < nvis ? p0 : 0.f;
+            p1 = j + 1 < nvis ? p1 : 0.f;
+          }
           w[e] = tc::pack2<__half>(p0, p1);
-          const float2 back = DT<__half>::to_f2(w[e]);
-          l += back.x + back.y;
+          const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+          l8[2 * e] += back.x;
+          l8[2 * e + 1] += back.y;
         }
-        *reinterpret_cast<uint4*>(prow + (cc / 8) * kRegion + row * 128 +
-                                  (((cc % 8) ^ (row % 8)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(prow + swz_off(row, cc)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
+      const float l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
       tc::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[s]);
-      if (i > 0) epilogue(i - 1, m_prev, l_prev, true);
-      m_prev = mx;
-      l_prev = l;
-      t_prev = t;
+      if (lane == 0) mbar_arrive(&bars->p_full[s]);  // P is ready for the P.V MMA
+      // epilogue of this tile: O / l in fp16 staged in the (consumed) P buffer
+      // and written with TMA stores; the base-2 lse with plain stores.  Both
+      // land tile-contiguous: block (c, b, kvh), rows (t, g).
+      if (!warp_wait(&bars->o_full[s], ph, bars, a.status, kSiteFull)) break;
+      tc::fence_after_sync();
+      const float inv = 1.f / l;
+#pragma unroll
+      for (int part = 0; part < D / 32; ++part)
+        tc::tmem_ld32(o_tm + part * 32, *reinterpret_cast<uint32_t(*)[32]>(r + part * 32));
+      tc::tmem_wait_ld();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->o_empty[s]);  // O may be overwritten by tile i + 2
+#pragma unroll
+      for (int v = 0; v < D / 8; ++v)
+        *reinterpret_cast<uint4*>(prow + swz_off(row, v)) = pack8<__half>(r + v * 8, inv);
+      if (t < a.T) a.part_lse[blk * TG + (size_t)t * G + row % G] = mx + log2f(l);
+      tc::fence_proxy_async_smem();
+      named_bar_sync(3 + grp, 128);
+      if (leader) {
+#pragma unroll
+        for (int rg = 0; rg < DR; ++rg)
+          tc::tma_store_3d(&map_po, rg * 64, t_first * G, (int)blk, prow + rg * kRegion);
+        tc::bulk_commit();
+      }
     }
-    (void)t_prev;
-    if (ntiles > 0 && !bars->abort) epilogue(ntiles - 1, m_prev, l_prev, true);
+    if (leader) tc::bulk_wait_all();
   }
 
   tc::fence_before_sync();
@@ -475,31 +490,54 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // out[b,t,h,:] = sum_c w_c 2^k_c o'_c / sum_c w_c, w_c = 2^(lse_c - max lse),
-// over the chunks c = 0 .. (len+t)/C that row sees.
-template <typename T>
-__global__ void prefill_combine_tc_kernel(const __half* __restrict__ part_o,
-                                          const float* __restrict__ part_lse,
-                                          const int* __restrict__ part_k, T* __restrict__ out,
-                                          LenArray len, int B, int T_, int Hq, int Hkv, int D,
-                                          int C) {
-  const size_t row = blockIdx.x;  // (b*T + t)*Hq + h
+// over the chunks c = 0 .. (len+t)/C that row sees.  D/8 threads per row, each
+// owning 8 consecutive outputs (16-byte loads of the fp16 partials).
+template <typename T, int D>
+__global__ void __launch_bounds__(128) prefill_combine_tc_kernel(
+    const __half* __restrict__ part_o, const float* __restrict__ part_lse,
+    const int* __restrict__ part_k, T* __restrict__ out, LenArray len, int B, int T_, int Hq,
+    int Hkv) {
+  constexpr int TPR = D / 8;            // threads per row
+  constexpr int RPB = 128 / TPR;        // rows per block
+  const size_t R = (size_t)B * T_ * Hq;
+  const int sub = threadIdx.x % TPR;
+  size_t row = (size_t)blockIdx.x * RPB + threadIdx.x / TPR;
+  const bool active = row < R;
+  if (!active) row = R - 1;             // keep every lane in the shuffles
   const int h = row % Hq;
   const int bt = row / Hq;
   const int t = bt % T_, b = bt / T_;
-  const int kh = b * Hkv + h / (Hq / Hkv);
-  const int last = (len.v[b] + t) / C;
-  const size_t R = (size_t)B * T_ * Hq;
+  const int G = Hq / Hkv;
+  const int kh = b * Hkv + h / G;
+  // partial row of (b, t, h) inside each chunk's R rows: block (b, kvh), row (t, g)
+  const size_t pr = (size_t)kh * T_ * G + (size_t)t * G + h % G;
+  const int last = (len.v[b] + t) / kC;
   float M = -INFINITY;
-  for (int c = 0; c <= last; ++c) M = fmaxf(M, part_lse[c * R + row]);
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float num = 0.f, den = 0.f;
-    for (int c = 0; c <= last; ++c) {
-      const float w = exp2f(part_lse[c * R + row] - M);
-      const float o = __half2float(part_o[(c * R + row) * D + d]);
-      num = fmaf(w * exp2f((float)part_k[(size_t)c * B * Hkv + kh]), o, num);
-      den += w;
+  for (int c = sub; c <= last; c += TPR) M = fmaxf(M, __ldg(part_lse + c * R + pr));
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float den = 0.f;
+#pragma unroll 4
+  for (int c = 0; c <= last; ++c) {
+    const float w = exp2f(__ldg(part_lse + c * R + pr) - M);
+    const float wk = ldexpf(w, __ldg(part_k + (size_t)c * B * Hkv + kh));
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(part_o + (c * R + pr) * D) + sub);
+    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+      acc[2 * e] = fmaf(wk, f.x, acc[2 * e]);
+      acc[2 * e + 1] = fmaf(wk, f.y, acc[2 * e + 1]);
     }
-    out[row * D + d] = DT<T>::from_f(num / den);
+    den += w;
+  }
+  if (active) {
+    const float inv = 1.f / den;
+    uint32_t r[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(acc[e]);
+    reinterpret_cast<uint4*>(out + row * D)[sub] = pack8<T>(r, inv);
   }
 }
 
@@ -511,16 +549,22 @@ cudaError_t launch_t(const TcArgs& args, const CUtensorMap& mq, const CUtensorMa
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        TcCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
+  CUtensorMap mpo;
+  if (!make_tmap_partial(&mpo, args.part_o, D, (uint64_t)args.T * G,
+                         (uint64_t)args.nchunks * args.B * args.Hkv))
+    return cudaErrorInvalidValue;
   const int units = args.B * args.Hkv * args.nchunks;
   timer.before(s);
-  k<<<units, kThreads, TcCfg<D>::kSmem, s>>>(mq, mx, mk, mv, args);
+  k<<<units, kThreads, TcCfg<D>::kSmem, s>>>(mq, mx, mk, mv, mpo, args);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   timer.after(s);
   LenArray len;
   for (int i = 0; i < kMaxBatch; ++i) len.v[i] = args.len[i];
-  prefill_combine_tc_kernel<T><<<args.B * args.T * args.Hq, D, 0, s>>>(
+  const size_t R = (size_t)args.B * args.T * args.Hq;
+  constexpr int RPB = 128 / (D / 8);
+  prefill_combine_tc_kernel<T, D><<<(unsigned)((R + RPB - 1) / RPB), 128, 0, s>>>(
       static_cast<const __half*>(args.part_o), args.part_lse, args.part_k, static_cast<T*>(out),
-      len, args.B, args.T, args.Hq, args.Hkv, D, kC);
+      len, args.B, args.T, args.Hq, args.Hkv);
   return cudaGetLastError();
 }
 
@@ -528,16 +572,16 @@ cudaError_t launch_t(const TcArgs& args, const CUtensorMap& mq, const CUtensorMa
 
 int prefill_tc_chunk_keys() { return kC; }
 
-// Q viewed as [tokens][Hq][D]: box (64 of D) x (G heads) x (128/G tokens).
-bool make_tmap_q(CUtensorMap* map, const void* q, int dtype, int D, int Hq, uint64_t tokens,
-                 int G, int TQ);
+bool prefill_supported(int dtype, int D, int G) {
+  return (dtype == DKV_BF16 || dtype == DKV_FP16) && (D == 64 || D == 128) &&
+         (G == 1 || G == 2 || G == 4 || G == 8);
+}
 
 cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, const void* wq, cudaStream_t s,
                               int* launches, const KernelTimer& timer) {
   const int G = p.Hq / p.Hkv;
   const int D = p.D;
-  if (p.H % 8 != 0 || (D != 64 && D != 128) || (G != 1 && G != 2 && G != 4 && G != 8))
-    return cudaErrorInvalidValue;
+  if (p.H % 8 != 0 || !prefill_supported(dtype, D, G)) return cudaErrorInvalidValue;
   // 1. Q projection (HBM-resident Q) on the tensor cores
   cudaError_t e = launch_gemm_tc(p.x, wq, const_cast<void*>(p.q), p.B * p.T, p.Hq * D, p.H,
                                  dtype, p.status, s);

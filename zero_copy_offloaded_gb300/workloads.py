@@ -99,6 +99,10 @@ WORKLOADS = {
         Workload("llama8b_decode", "decode", B=8, H=4096, Hq=32, Hkv=8, D=128, P=32768),
         Workload("llama8b_prefill", "prefill", B=1, H=4096, Hq=32, Hkv=8, D=128,
                  P=28672, T=4096),
+        # a quarter-size chunked prefill (same heads), small enough for a
+        # full profiler capture
+        Workload("llama8b_prefill_quarter", "prefill", B=1, H=4096, Hq=32, Hkv=8, D=128,
+                 P=7168, T=1024),
         Workload("longctx_b1_s16k", "decode", B=1, H=4096, Hq=32, Hkv=8, D=128,
                  P=16384, spike_frac=0.01),
         Workload("longctx_b1_s64k", "decode", B=1, H=4096, Hq=32, Hkv=8, D=128,
