@@ -1,0 +1,36 @@
+"""Failure detection without faulting the GPU: a bounded device-side wait
+that nothing completes gives up after about a second, the kernel returns,
+the host reads DKV_ERR_TIMEOUT from the status word, and the next call on
+the same context is correct."""
+import numpy as np
+import pytest
+
+from zero_copy_offloaded_gb300 import workloads as wl
+
+from .helpers import Case, assert_close, out_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def test_withheld_tile_times_out_then_recovers():
+    import zero_copy_offloaded_gb300 as dkv
+    w = wl.Workload("t", "decode", B=2, H=128, Hq=8, Hkv=2, D=128, P=700, seed=31)
+    case = Case(w)
+    try:
+        dkv.dkv_cache_debug_withhold(case.cache.h, True)
+        out = case.out_tensor(1)
+        case.cache.decode(case.x.reshape(w.B, 1, w.H), case.wq, case.wk, case.wv, w.Hq, out)
+        with pytest.raises(dkv.DkvError) as ei:
+            case.cache.sync()
+        assert ei.value.name == "DKV_ERR_TIMEOUT"
+        # the status word was cleared by the read; the prefix is intact
+        assert np.array_equal(case.cache.k_host[:, :, : w.P], case.k0[:, :, : w.P])
+        dkv.dkv_cache_debug_withhold(case.cache.h, False)
+        case.cache.set_lengths(case.lens.astype(np.int32))
+        out = case.run_decode()
+        ref = case.oracle()
+        assert_close(out_f64(out, w.dtype).reshape(w.B, w.Hq, w.D),
+                     ref["out"].reshape(w.B, w.Hq, w.D), "after recovery")
+        case.cache.sync()  # no stale timeout left behind
+    finally:
+        case.free()

@@ -94,6 +94,7 @@ def lib(build_if_missing: bool = False):
         "dkv_cache_last_kernel_ms": [P, ctypes.POINTER(ctypes.c_float)],
         "dkv_decode_noalloc": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P],
         "dkv_project": [P, P, P, I, I, I, I, P],
+        "dkv_cache_debug_withhold": [P, I],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -193,6 +194,10 @@ def dkv_cache_reserve(h, n_q_heads, max_new_tokens):
 
 def dkv_cache_set_tuning(h, splits=0, tile_n=0, stages=0):
     _check(lib().dkv_cache_set_tuning(h, splits, tile_n, stages), "dkv_cache_set_tuning")
+
+
+def dkv_cache_debug_withhold(h, enable=True):
+    _check(lib().dkv_cache_debug_withhold(h, int(bool(enable))), "dkv_cache_debug_withhold")
 
 
 def dkv_cache_kernel_timing(h, enable=True):

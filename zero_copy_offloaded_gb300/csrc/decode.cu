@@ -236,7 +236,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
           cp_async16(kt + dst, kg + src, 16);
           cp_async16(vt + dst, vg + src, 16);
         }
-        cp_async_arrive_noinc(&full[stage]);
+        // (the test hook withholds the first tile's signal: the consumers'
+        // bounded wait then expires and reports a timeout)
+        if (!(p.debug_withhold && it == 0)) cp_async_arrive_noinc(&full[stage]);
       }
     }
     cp_async_wait_all();

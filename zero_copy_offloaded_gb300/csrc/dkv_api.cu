@@ -79,6 +79,7 @@ struct dkv_cache {
   int tune_splits, tune_tile, tune_stages;
   KernelTimer timer;      // events around the main fused kernel (measurement)
   bool timer_used;
+  int debug_withhold;     // test hook for the bounded-wait path
   std::mutex mu;
 };
 
@@ -217,6 +218,7 @@ dkv_status decode_impl(dkv_cache* c, const void* x, const void* wq, const void* 
   p.B = B; p.H = hidden; p.Hq = Hq; p.Hkv = c->Hkv; p.D = D; p.S_max = c->max_tokens;
   p.splits = ch.splits; p.tile_n = ch.tile_n; p.stages = ch.stages;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  p.debug_withhold = c->debug_withhold;
   fill_lens(p.len, c->len);
   g_last_launches = 0;
   cudaError_t e = launch_decode(p, c->dtype, ch.grid, ch.smem, s, &g_last_launches, c->timer);
@@ -324,6 +326,7 @@ dkv_status dkv_cache_alloc(dkv_cache** out, int batch, int n_kv_heads, int head_
   c->sms = sms;
   c->tune_splits = c->tune_tile = c->tune_stages = 0;
   c->timer_used = false;
+  c->debug_withhold = 0;
   *out = c;
   return DKV_OK;
 }
@@ -386,6 +389,12 @@ dkv_status dkv_cache_info(const dkv_cache* c, dkv_cache_info_t* info) {
   info->device_staging_bytes = 0;
   info->batch = c->B; info->n_kv_heads = c->Hkv; info->head_dim = c->D;
   info->max_tokens = c->max_tokens; info->dtype = c->dtype;
+  return DKV_OK;
+}
+
+dkv_status dkv_cache_debug_withhold(dkv_cache* c, int enable) {
+  if (!valid(c)) return fail(DKV_ERR_INVALID_ARG, "invalid cache handle");
+  c->debug_withhold = enable ? 1 : 0;
   return DKV_OK;
 }
 

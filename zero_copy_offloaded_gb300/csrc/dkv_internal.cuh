@@ -177,6 +177,7 @@ struct DecodeParams {
   int tile_n;      // keys per tile
   int stages;
   float scale_log2;  // log2(e) / sqrt(D)
+  int debug_withhold;  // test hook: producers never signal their first tile
   int len[kMaxBatch];
 };
 
