@@ -51,7 +51,101 @@ def parse():
     ap.add_argument("--no-extras", action="store_true",
                     help="only the headline decode (no baselines, prefill, oracle timing)")
     ap.add_argument("--prefill-only", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="one JSON line per workload: every decode workload with its naive and "
+                         "copy-to-HBM baselines, then every prefill workload")
     return ap.parse_args()
+
+
+def sweep(args, dkv, torch, dev, stream, flush, pk):
+    """All workloads, one JSON line each (secondary measurements, not the headline)."""
+    # link denominators over a 1 GiB mapped buffer
+    probe = dkv.KVCache(1, 8, 128, 262144, "bf16")
+    kd, _ = dkv.dkv_cache_device_ptrs(probe.h)
+    sink = torch.zeros(4, dtype=torch.int32, device=dev)
+    nbytes = 8 * 262144 * 128 * 2
+    best = min(_time_once(torch, stream, flush,
+                          lambda: dkv.dkv_probe_read(kd, nbytes, sink, stream)) for _ in range(3))
+    link_rd = nbytes / (best * 1e-3) / 1e9
+    probe.free()
+    pinned = torch.empty(256 << 20, dtype=torch.uint8, pin_memory=True)
+    best = min(_time_once(torch, stream, flush,
+                          lambda: dkv.dkv_probe_write(pinned.data_ptr(), pinned.numel(), stream))
+               for _ in range(3))
+    link_wr = pinned.numel() / (best * 1e-3) / 1e9
+    hbm = pk.get("hbm_gbs") or 6800.0
+    print(json.dumps({"sweep": "link", "zero_copy_read_gbs": link_rd,
+                      "zero_copy_write_gbs": link_wr}), flush=True)
+    for name, w in wl.WORKLOADS.items():
+        if w.phase != "decode":
+            continue
+        tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+        cache = dkv.KVCache(w.B, w.Hkv, w.D, w.S_max, w.dtype)
+        wl.fill_cache(w, cache.k_host, cache.v_host)
+        dense = wl.make_dense(w)
+        x, wq, wk, wv = (torch.from_numpy(dense[k].view(np.int16)).view(tdt).to(dev)
+                         for k in ("x", "wq", "wk", "wv"))
+        x = x.reshape(w.B, 1, w.H)
+        out = torch.empty((w.B, 1, w.Hq, w.D), dtype=tdt, device=dev)
+        lens = np.full(w.B, w.P, np.int32)
+        dkv.dkv_cache_kernel_timing(cache.h, True)
+
+        def step():
+            cache.set_lengths(lens)
+            cache.decode(x, wq, wk, wv, w.Hq, out, stream)
+        for _ in range(3):
+            step()
+        ms = [_time_once(torch, stream, flush, step) for _ in range(max(args.steps, 5))]
+        kern = dkv.dkv_cache_last_kernel_ms(cache.h)
+        q = torch.randn((w.B, w.Hq, w.D), device=dev).to(tdt)
+        o2 = torch.empty_like(q)
+        cache.set_lengths(lens)
+        naive = min(_time_once(torch, stream, flush,
+                               lambda: dkv.dkv_attend_naive(cache.h, q, w.Hq, o2, stream))
+                    for _ in range(3))
+        cbytes = w.B * w.Hkv * w.S_max * w.D * 2
+        ks = torch.empty(cbytes, dtype=torch.uint8, device=dev)
+        vs = torch.empty(cbytes, dtype=torch.uint8, device=dev)
+
+        def staged():
+            cache.set_lengths(lens)
+            dkv.dkv_decode_staged(cache.h, x, wq, wk, wv, w.H, w.Hq, out, ks, vs, stream)
+        staged_ms = min(_time_once(torch, stream, flush, staged) for _ in range(3))
+        del ks, vs
+        cache.free()
+        step_ms = statistics.median(ms)
+        hb = w.host_read_bytes()
+        print(json.dumps({
+            "sweep": name, "phase": "decode", "B": w.B, "P": w.P, "D": w.D, "Hq": w.Hq,
+            "Hkv": w.Hkv, "dtype": w.dtype, "step_ms": step_ms, "tok_s": w.B / (step_ms * 1e-3),
+            "fused_kernel_ms": kern, "host_link_gbs": hb / (kern * 1e-3) / 1e9,
+            "frac_of_link": hb / (kern * 1e-3) / 1e9 / link_rd,
+            "naive_zero_copy_ms": naive, "copy_to_hbm_then_attend_ms": staged_ms}), flush=True)
+    for name, w in wl.WORKLOADS.items():
+        if w.phase != "prefill":
+            continue
+        a2 = argparse.Namespace(**vars(args))
+        a2.prefill_workload = name
+        res = bench_prefill(a2, dkv, torch, dev, stream, flush, pk, link_rd, link_wr, hbm)
+        print(json.dumps({"sweep": name, "phase": "prefill", **res}), flush=True)
+
+
+def kernel_source_hash(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "zero_copy_offloaded_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(key, files):
+    """Per-launch traffic from a committed ncu capture, if it was taken on the
+    kernel sources as they are now (else None)."""
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))[key]
+    except Exception:
+        return None
+    return rec if rec.get("src_sha256_16") == kernel_source_hash(files) else None
 
 
 def peaks():
@@ -196,6 +290,8 @@ def main():
 
     pk = peaks()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    if args.sweep:
+        return sweep(args, dkv, torch, dev, stream, flush, pk)
     if args.prefill_only:
         # prefill alone (profiling aid): link/HBM rates from the probes, then the prefill
         probe_cache = dkv.KVCache(1, 8, 128, 65536, "bf16")
@@ -296,8 +392,12 @@ def main():
 
     host_bytes = w.host_read_bytes()
     achieved = host_bytes / (fused_ms * 1e-3) / 1e9
+    tr = ncu_traffic(f"decode_fused_kernel/{w.name}", ["decode.cu", "dkv_internal.cuh"])
     roofline = {"bound": "host_link", "achieved": achieved, "peak": link_rd, "unit": "GB/s",
-                "frac": achieved / link_rd, "traffic": None,
+                "frac": achieved / link_rd,
+                # host-link bytes (sysmem sectors x 32 B) of one launch from ncu; HBM bytes beside
+                "traffic": tr["host_link_bytes"] if tr else None,
+                "traffic_dram": tr["dram_bytes"] if tr else None,
                 "peak_source": "zero-copy streaming read probe over the same cache, same run",
                 "kernel": "decode_fused_kernel", "kernel_ms": fused_ms,
                 "algorithmic_bytes_per_launch": host_bytes}
