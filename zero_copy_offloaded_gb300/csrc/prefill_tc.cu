@@ -7,27 +7,27 @@
 // consumed there (Key Ideas (2)); warps specialise into loading, computing and
 // storing roles (Key Ideas (3)).
 //
-// One CTA = one unit (sequence b, KV head, chunk of C = 128 keys).
+// One CTA = one unit (sequence b, KV head, chunk of C = 256 keys).
 //   1. The chunk's K and V land in shared memory (128-byte swizzled rows):
 //      cached rows with 16-byte cp.async from the mapped host cache (each host
 //      byte crosses the link once), new rows from a tcgen05 GEMM
-//      [x rows] . [Wk | Wv] (TMA-fed, accumulator in TMEM) whose epilogue
-//      rounds them, writes them into the stationary tile and appends them to
-//      the host cache.
+//      [x rows] . [Wk | Wv] (TMA-fed, accumulator in TMEM, 128 rows per pass)
+//      whose epilogue rounds them, writes them into the stationary tile and
+//      appends them to the host cache.
 //   2. Every Q tile of the KV group that can see the chunk (128 rows = 128/G
-//      tokens x G heads, TMA from HBM) runs S = Q.K^T (tcgen05, TMEM), a
-//      complete softmax over the chunk (it is stationary, so there is no
-//      running rescale), O = P.V (tcgen05, TMEM, fp16 operands), and its
-//      normalised O and base-2 log-sum-exp are written as the chunk's
-//      partial.  Two softmax warpgroups take alternate Q tiles, each with its
-//      own S and O in TMEM and its own P tile in shared memory, so the tensor
-//      cores run one group's MMAs while the other group does its softmax.
+//      tokens x G heads, TMA from HBM) runs S = Q.K^T (tcgen05, N = 256, TMEM),
+//      a complete softmax over the chunk (it is stationary, so there is no
+//      running rescale), O = P.V (tcgen05 with P as the TMEM operand, fp16),
+//      and its normalised O (staged in shared memory, TMA store) and base-2
+//      log-sum-exp are written as the chunk's partial.  S of tile i+1 is
+//      computed while the softmax of tile i runs.
 // A combine kernel merges the chunks' partials per query row.
 //
 // Warp roles (320 threads): warp 0 loads (TMA / cp.async), warp 1 allocates
-// TMEM and issues every MMA from one thread, warps 2-5 and 6-9 are the two
-// softmax / epilogue groups (one TMEM lane = one row per thread).  Every wait
-// is bounded.
+// TMEM and issues every MMA from one thread, warps 2-9 are the softmax /
+// epilogue warps: two per TMEM lane quarter, each owning half of a row's 256
+// scores (the halves exchange their max and sum through shared memory).
+// Every wait is bounded.
 #include "tc_common.cuh"
 
 namespace dkv {
@@ -40,37 +40,56 @@ bool make_tmap_partial(CUtensorMap* map, void* base, int D, uint64_t rows, uint6
 
 namespace {
 
-constexpr int kC = 128;        // keys per stationary chunk
+constexpr int kC = 256;        // keys per stationary chunk
 constexpr int kBQ = 128;       // rows per Q tile
 constexpr int kThreads = 320;  // 10 warps
-constexpr int kRegion = 128 * 128;  // one 128-row x 128-byte swizzled region
+constexpr int kRegKV = kC * 128;   // one 256-row x 128-byte swizzled region (K or V)
+constexpr int kRegQ = kBQ * 128;   // one 128-row x 128-byte swizzled region
+// TMEM columns
+constexpr uint32_t kTmS = 0;       // S: 256 fp32 columns
+constexpr uint32_t kTmO = 256;     // O: D fp32 columns
+constexpr uint32_t kTmP = 384;     // P: 256 fp16 keys, two per column
 
 template <int D>
 struct TcCfg {
   static constexpr int DR = D / 64;                    // 128-byte regions per row
-  static constexpr int kKV = kC * D * 2;               // one of K or V
-  static constexpr int kQ = kBQ * D * 2;               // one Q tile
-  static constexpr int kP = kBQ * kC * 2;              // one P tile
+  static constexpr int kKV = DR * kRegKV;              // one of K or V
+  static constexpr int kQ = DR * kRegQ;                // one Q tile
+  static constexpr int kO = DR * kRegQ;                // output staging (128 rows)
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKV;
   static constexpr int kOffQ = kOffV + kKV;            // two Q buffers
-  static constexpr int kOffP = kOffQ + 2 * kQ;         // two P buffers
-  static constexpr int kOffBar = kOffP + 2 * kP;
-  // projection staging (aliases the Q and P buffers): x block [128 x 64] and
-  // W block [64 x 2D], two stages
+  static constexpr int kOffO = kOffQ + 2 * kQ;
+  // projection staging (aliases the Q buffers and the output staging): x block
+  // [128 x 64] and W block [64 x 2D], two stages
   static constexpr int kProjA = kBQ * 64 * 2;          // 16 KB
   static constexpr int kProjB = 64 * 2 * D * 2;        // 16 / 32 KB
   static constexpr int kProjStage = kProjA + kProjB;
-  static_assert(2 * kProjStage <= 2 * kQ + 2 * kP, "projection staging must fit");
-  static constexpr int kSmem = 1024 + kOffBar + 256;
+  static constexpr int kEnd = (kOffO + kO) > (kOffQ + 2 * kProjStage) ? (kOffO + kO)
+                                                                       : (kOffQ + 2 * kProjStage);
+  static constexpr int kOffBar = kEnd;
 };
 
+constexpr int kSmemLimit = 232448;  // 227 KB of dynamic shared memory per CTA
+
+template <int D>
+constexpr int smem_request() {
+  // tiles + barrier block + up to 1 KB to align the tiles to 1024 bytes, capped
+  // at the per-CTA limit (the kernel checks the padding it actually needs)
+  return (TcCfg<D>::kEnd + 4096 + 1024) < kSmemLimit ? (TcCfg<D>::kEnd + 4096 + 1024)
+                                                      : kSmemLimit;
+}
+
 struct Bars {
-  uint64_t q_full[2], q_empty[2], s_full[2], s_empty[2], p_full[2], p_empty[2], o_full[2],
-      o_empty[2], kv_host, kv_ready, pr_full[2], pr_empty[2], pr_done;
+  uint64_t q_full[2], q_empty[2], s_full, s_empty, p_full, p_empty, o_full, o_empty, kv_host,
+      kv_ready, pr_full[2], pr_empty[2], pr_done, pr_drain;
+  uint64_t xsync[3];  // softmax-warp rendezvous points of a tile (8 warps each)
+  uint64_t vsync;     // rendezvous of the four warps converting V
   uint32_t tmem_base;
   volatile int abort;
   float vmax[4];
+  float xmax[2][kBQ];  // the two halves' row maxima
+  float xl[2][kBQ];    // the two halves' row sums
 };
 
 struct TcArgs {
@@ -78,8 +97,8 @@ struct TcArgs {
   const void* v_read;
   void* k_host;
   void* v_host;
-  void* part_o;     // [nchunks, B*T*Hq, D] fp16, normalised, times 2^-k of the chunk
-  float* part_lse;  // [nchunks, B*T*Hq]
+  void* part_o;     // [nchunks, B, Hkv, T, G, D] fp16, normalised, times 2^-k of the chunk
+  float* part_lse;  // [nchunks, B, Hkv, T, G]
   int* part_k;      // [nchunks, B*Hkv]
   DeviceStatus* status;
   int B, T, H, Hq, Hkv, S_max, nchunks;
@@ -95,14 +114,24 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
   return false;
 }
 
-// Warp-uniform bounded wait (tcgen05.ld after it needs the whole warp).
+// Warp-uniform bounded wait (tcgen05.ld / st after it need the whole warp).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Bars* bars,
                                           DeviceStatus* st, int site) {
   return __all_sync(0xffffffffu, wait_or_abort(bar, parity, bars, st, site));
 }
 
-__device__ __forceinline__ int swz_off(int row, int cc) {  // 16-byte chunk cc of a row
-  return (cc / 8) * kRegion + row * 128 + (((cc % 8) ^ (row % 8)) * 16);
+// A rendezvous of several warps on an mbarrier (one arrival per warp), bounded
+// like every other wait so that a warp that gave up cannot strand the others.
+__device__ __forceinline__ bool warps_sync(uint64_t* bar, uint32_t parity, Bars* bars,
+                                           DeviceStatus* st) {
+  __syncwarp();
+  if (threadIdx.x % 32 == 0) mbar_arrive(bar);
+  return warp_wait(bar, parity, bars, st, kSiteFull);
+}
+
+// 16-byte chunk cc of row `row` in a tile of 128-byte swizzled regions of `reg` bytes.
+__device__ __forceinline__ int swz(int row, int cc, int reg) {
+  return (cc / 8) * reg + row * 128 + (((cc % 8) ^ (row % 8)) * 16);
 }
 
 template <typename T>
@@ -128,10 +157,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
+  {
+    // the 128-byte swizzle needs 1024-byte aligned tiles; if the padding that
+    // takes does not fit in what was launched, report it and touch nothing
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    const uint32_t pad = (uint32_t)(smem - smem_raw);
+    if (pad + Cfg::kOffBar + sizeof(Bars) > dyn) {
+      if (threadIdx.x == 0) record_timeout(a.status, kSiteGridBarrier);
+      return;
+    }
+  }
   uint8_t* ks = smem + Cfg::kOffK;
   uint8_t* vs = smem + Cfg::kOffV;
   uint8_t* qs = smem + Cfg::kOffQ;
-  uint8_t* ps = smem + Cfg::kOffP;
+  uint8_t* os = smem + Cfg::kOffO;
   Bars* bars = reinterpret_cast<Bars*>(smem + Cfg::kOffBar);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -144,7 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (k0 >= S) return;  // uniform over the CTA, before any barrier
   const int nkeys = min(kC, S - k0);
   const int nhost = max(0, min(kC, P - k0));   // rows [0, nhost) come from the host cache
-  const bool has_new = k0 + kC > P;            // rows [P - k0, C) are projected here
+  const bool has_new = k0 + kC > P;            // rows [nhost, C) are projected here
+  const int pass0 = nhost / 128;               // first 128-row projection pass with new rows
+  const int npass = has_new ? 2 - pass0 : 0;
   const int t_lo = max(0, k0 - P);             // first token that sees this chunk
   const int ntiles = (a.T - t_lo + TQ - 1) / TQ;
 
@@ -152,18 +194,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_empty[i], 4);
-      mbar_init(&bars->p_full[i], 4);
-      mbar_init(&bars->p_empty[i], 1);
-      mbar_init(&bars->o_full[i], 1);
-      mbar_init(&bars->o_empty[i], 4);
       mbar_init(&bars->pr_full[i], 1);
       mbar_init(&bars->pr_empty[i], 1);
     }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_empty, 8);
+    mbar_init(&bars->p_full, 8);
+    mbar_init(&bars->p_empty, 1);
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->o_empty, 8);
     mbar_init(&bars->kv_host, 32);
     mbar_init(&bars->kv_ready, 8);
     mbar_init(&bars->pr_done, 1);
+    mbar_init(&bars->pr_drain, 8);
+    for (int i = 0; i < 3; ++i) mbar_init(&bars->xsync[i], 8);
+    mbar_init(&bars->vsync, 4);
     bars->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -172,8 +217,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
-  // TMEM columns: S[0] 0..127, S[1] 128..255, O[0] 256.., O[1] 384..; the
-  // projection accumulator (2D columns) reuses 0..2D-1 before the Q loop.
   const int nk_proj = (a.H + 63) / 64;  // TMA zero-fills past H
   const size_t head_off = ((size_t)b * a.Hkv + kvh) * a.S_max * D;
 
@@ -187,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rows = has_new ? nhost : kC;  // zero-fill the tail when nothing is projected
       for (int i = lane; i < rows * CPR; i += 32) {
         const int r = i / CPR, cc = i % CPR;
-        const int off = swz_off(r, cc);
+        const int off = swz(r, cc, kRegKV);
         const bool ok = r < nhost;
         const size_t src = ok ? (size_t)r * D + cc * 8 : 0;
         cp_async16(ks + off, kg + src, ok ? 16 : 0);
@@ -197,31 +240,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) {
       tc::prefetch_tmap(&map_q);
-      // (b) projection operands for the new rows: x rows and [Wk | Wv] columns
+      // (b) projection operands, one 128-row pass at a time: x rows, [Wk | Wv]
       if (has_new) {
         tc::prefetch_tmap(&map_x);
         tc::prefetch_tmap(&map_wk);
         tc::prefetch_tmap(&map_wv);
-        const int xrow = b * a.T + (k0 - P);  // may be negative: TMA fills zeros
-        for (int kb = 0; kb < nk_proj; ++kb) {
-          const int s = kb & 1;
-          if (!wait_or_abort(&bars->pr_empty[s], ((kb >> 1) & 1) ^ 1, bars, a.status, kSiteEmpty))
-            break;
-          uint8_t* pa = qs + s * Cfg::kProjStage;
-          uint8_t* pb = pa + Cfg::kProjA;
-          tc::mbar_expect_tx(&bars->pr_full[s], Cfg::kProjStage);
-          tc::tma_load_2d(pa, &map_x, kb * 64, xrow, &bars->pr_full[s]);
+        for (int ps = 0; ps < npass; ++ps) {
+          const int xrow = b * a.T + (k0 + (pass0 + ps) * 128 - P);  // may be negative: zeros
+          for (int kb = 0; kb < nk_proj; ++kb) {
+            const int g = ps * nk_proj + kb;
+            const int s = g & 1;
+            if (!wait_or_abort(&bars->pr_empty[s], ((g >> 1) & 1) ^ 1, bars, a.status, kSiteEmpty))
+              break;
+            uint8_t* pa = qs + s * Cfg::kProjStage;
+            uint8_t* pb = pa + Cfg::kProjA;
+            tc::mbar_expect_tx(&bars->pr_full[s], Cfg::kProjStage);
+            tc::tma_load_2d(pa, &map_x, kb * 64, xrow, &bars->pr_full[s]);
 #pragma unroll
-          for (int r = 0; r < DR; ++r) {
-            tc::tma_load_2d(pb + r * 8192, &map_wk, kvh * D + r * 64, kb * 64, &bars->pr_full[s]);
-            tc::tma_load_2d(pb + (DR + r) * 8192, &map_wv, kvh * D + r * 64, kb * 64,
-                            &bars->pr_full[s]);
+            for (int r = 0; r < DR; ++r) {
+              tc::tma_load_2d(pb + r * 8192, &map_wk, kvh * D + r * 64, kb * 64,
+                              &bars->pr_full[s]);
+              tc::tma_load_2d(pb + (DR + r) * 8192, &map_wv, kvh * D + r * 64, kb * 64,
+                              &bars->pr_full[s]);
+            }
           }
         }
-        // the Q buffers alias the projection staging: wait until it is consumed
-        wait_or_abort(&bars->pr_done, 0, bars, a.status, kSiteFull);
+        // the Q buffers alias the projection staging: wait until every pass
+        // has consumed it (phases in order: a parity wait on a phase that has
+        // not started yet would return at once)
+        for (int ps = 0; ps < npass; ++ps)
+          if (!wait_or_abort(&bars->pr_done, ps & 1, bars, a.status, kSiteFull)) break;
       }
-      // (c) Q tiles
+      // (c) Q tiles, double-buffered
       for (int i = 0; i < ntiles && !bars->abort; ++i) {
         const int s = i & 1;
         if (!wait_or_abort(&bars->q_empty[s], ((i >> 1) & 1) ^ 1, bars, a.status, kSiteEmpty))
@@ -230,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_expect_tx(&bars->q_full[s], Cfg::kQ);
 #pragma unroll
         for (int r = 0; r < DR; ++r)
-          tc::tma_load_3d(qs + s * Cfg::kQ + r * kRegion, &map_q, r * 64, kvh * G, tok,
+          tc::tma_load_3d(qs + s * Cfg::kQ + r * kRegQ, &map_q, r * 64, kvh * G, tok,
                           &bars->q_full[s]);
       }
     }
@@ -239,99 +289,108 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================= MMA
     if (lane == 0) {
       const bool bf = DT<T>::code == DKV_BF16;
-      // projection: [128 x H] . [H x 2D] -> TMEM columns 0..2D-1
+      // projection passes: [128 x H] . [H x 2D] -> TMEM columns 0..2D-1
       if (has_new) {
         const uint32_t idesc = tc::idesc_f16(bf, 128, 2 * D, false, true);
-        for (int kb = 0; kb < nk_proj; ++kb) {
-          const int s = kb & 1;
-          if (!wait_or_abort(&bars->pr_full[s], (kb >> 1) & 1, bars, a.status, kSiteFull)) break;
+        for (int ps = 0; ps < npass && !bars->abort; ++ps) {
+          if (ps > 0 &&  // the softmax warps have drained the previous pass
+              !wait_or_abort(&bars->pr_drain, (ps - 1) & 1, bars, a.status, kSiteEmpty))
+            break;
           tc::fence_after_sync();
-          const uint32_t pa = smem_u32(qs + s * Cfg::kProjStage);
-          const uint32_t pb = pa + Cfg::kProjA;
+          for (int kb = 0; kb < nk_proj; ++kb) {
+            const int g = ps * nk_proj + kb;
+            const int s = g & 1;
+            if (!wait_or_abort(&bars->pr_full[s], (g >> 1) & 1, bars, a.status, kSiteFull)) break;
+            tc::fence_after_sync();
+            const uint32_t pa = smem_u32(qs + s * Cfg::kProjStage);
+            const uint32_t pb = pa + Cfg::kProjA;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc::mma_ss(tmem, tc::sdesc_sw128(pa + kk * 32, 16, 1024),
-                       tc::sdesc_sw128(pb + kk * 2048, 8192, 1024), idesc, (kb | kk) != 0);
-          tc::mma_commit(&bars->pr_empty[s]);
+            for (int kk = 0; kk < 4; ++kk)
+              tc::mma_ss(tmem, tc::sdesc_sw128(pa + kk * 32, 16, 1024),
+                         tc::sdesc_sw128(pb + kk * 2048, 8192, 1024), idesc, (kb | kk) != 0);
+            tc::mma_commit(&bars->pr_empty[s]);
+          }
+          tc::mma_commit(&bars->pr_done);
         }
-        tc::mma_commit(&bars->pr_done);
       }
       // the stationary K/V tile is complete (host rows landed, new rows written)
       wait_or_abort(&bars->kv_ready, 0, bars, a.status, kSiteFull);
       tc::fence_after_sync();
-      const uint32_t idesc_s = tc::idesc_f16(bf, 128, kC, false, false);  // Q.K^T
+      const uint32_t idesc_s = tc::idesc_f16(bf, 128, kC, false, false);  // Q.K^T, N = 256
       const uint32_t idesc_o = tc::idesc_f16(false, 128, D, false, true); // P.V in fp16
       const uint32_t ka = smem_u32(ks), va = smem_u32(vs);
-      auto issue_pv = [&](int j) {
-        const int s = j & 1;
-        if (!wait_or_abort(&bars->p_full[s], (j >> 1) & 1, bars, a.status, kSiteFull)) return;
-        if (!wait_or_abort(&bars->o_empty[s], ((j >> 1) & 1) ^ 1, bars, a.status, kSiteEmpty))
-          return;
-        tc::fence_after_sync();
-        const uint32_t pa = smem_u32(ps + s * Cfg::kP);
-        const uint32_t o_tm = tmem + 256 + s * 128;
-#pragma unroll
-        for (int kk = 0; kk < kC / 16; ++kk)
-          tc::mma_ss(o_tm, tc::sdesc_sw128(pa + (kk / 4) * kRegion + (kk % 4) * 32, 16, 1024),
-                     tc::sdesc_sw128(va + kk * 2048, kRegion, 1024), idesc_o, kk != 0);
-        tc::mma_commit(&bars->o_full[s]);
-        tc::mma_commit(&bars->p_empty[s]);
-      };
-      for (int i = 0; i < ntiles && !bars->abort; ++i) {
+      auto issue_s = [&](int i) -> bool {
         const int s = i & 1;
-        if (!wait_or_abort(&bars->q_full[s], (i >> 1) & 1, bars, a.status, kSiteFull)) break;
-        if (!wait_or_abort(&bars->s_empty[s], ((i >> 1) & 1) ^ 1, bars, a.status, kSiteEmpty))
-          break;
+        if (!wait_or_abort(&bars->q_full[s], (i >> 1) & 1, bars, a.status, kSiteFull)) return false;
+        // S of tile i-1 has been read by the softmax warps
+        if (!wait_or_abort(&bars->s_empty, (i & 1) ^ 1, bars, a.status, kSiteEmpty)) return false;
         tc::fence_after_sync();
         const uint32_t qa = smem_u32(qs + s * Cfg::kQ);
-        const uint32_t s_tm = tmem + s * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma_ss(s_tm, tc::sdesc_sw128(qa + (kk / 4) * kRegion + (kk % 4) * 32, 16, 1024),
-                     tc::sdesc_sw128(ka + (kk / 4) * kRegion + (kk % 4) * 32, 16, 1024), idesc_s,
+          tc::mma_ss(tmem + kTmS,
+                     tc::sdesc_sw128(qa + (kk / 4) * kRegQ + (kk % 4) * 32, 16, 1024),
+                     tc::sdesc_sw128(ka + (kk / 4) * kRegKV + (kk % 4) * 32, 16, 1024), idesc_s,
                      kk != 0);
-        tc::mma_commit(&bars->s_full[s]);
+        tc::mma_commit(&bars->s_full);
         tc::mma_commit(&bars->q_empty[s]);
-        if (i > 0) issue_pv(i - 1);
+        return true;
+      };
+      if (ntiles > 0) issue_s(0);
+      for (int i = 0; i < ntiles && !bars->abort; ++i) {
+        if (i + 1 < ntiles && !issue_s(i + 1)) break;
+        // P of tile i is in TMEM and O has been read out for tile i-1
+        if (!wait_or_abort(&bars->p_full, i & 1, bars, a.status, kSiteFull)) break;
+        if (!wait_or_abort(&bars->o_empty, (i & 1) ^ 1, bars, a.status, kSiteEmpty)) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk)
+          tc::mma_ts(tmem + kTmO, tmem + kTmP + kk * 8,
+                     tc::sdesc_sw128(va + kk * 2048, kRegKV, 1024), idesc_o, kk != 0);
+        tc::mma_commit(&bars->o_full);
+        tc::mma_commit(&bars->p_empty);
       }
-      if (ntiles > 0 && !bars->abort) issue_pv(ntiles - 1);
     }
     __syncwarp();
   } else {
-    // ============================================ two softmax / epilogue groups
-    const int grp = (warp - 2) / 4;           // group g takes tiles i with i % 2 == g
+    // ============================================= softmax / epilogue warps
+    const int hh = (warp - 2) / 4;            // which half of the 256 scores this warp owns
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;      // tile row = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int hrow = hh * 128 + row;          // this thread's row in a 256-row K/V tile
 
-    // (a) projection epilogue: group 0 takes the K columns, group 1 the V
-    //     columns; round, write into the stationary tile, append to the host.
-    if (has_new) {
-      const bool ok = warp_wait(&bars->pr_done, 0, bars, a.status, kSiteFull);
+    // (a) projection epilogue per pass: half 0 takes the K columns, half 1
+    //     the V columns; round, write into the stationary tile, append.
+    for (int ps = 0; ps < npass; ++ps) {
+      const bool ok = warp_wait(&bars->pr_done, ps & 1, bars, a.status, kSiteFull);
       tc::fence_after_sync();
-      if (ok) {
-        const int key = k0 + row;
-        const bool mine = row >= P - k0;      // this row is a new key projected here
-        const bool append = mine && key < S;
-        uint8_t* tile = grp ? vs : ks;
-        T* host = static_cast<T*>(grp ? a.v_host : a.k_host) + head_off + (size_t)key * D;
+      if (!ok) break;
+      const int r = (pass0 + ps) * 128 + row;  // key row within the chunk
+      const int key = k0 + r;
+      const bool mine = r >= nhost;            // this row is a new key projected here
+      const bool append = mine && key < S;
+      uint8_t* tile = hh ? vs : ks;
+      T* host = static_cast<T*>(hh ? a.v_host : a.k_host) + head_off + (size_t)key * D;
 #pragma unroll 1
-        for (int part = 0; part < D / 32; ++part) {
-          uint32_t r[32];
-          tc::tmem_ld32(tmem + lane_off + grp * D + part * 32, r);
-          tc::tmem_wait_ld();
+      for (int part = 0; part < D / 32; ++part) {
+        uint32_t v[32];
+        tc::tmem_ld32(tmem + lane_off + hh * D + part * 32, v);
+        tc::tmem_wait_ld();
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const uint4 o = pack8<T>(r + v * 8, 1.f);
-            if (mine) *reinterpret_cast<uint4*>(tile + swz_off(row, part * 4 + v)) = o;
-            if (append) *reinterpret_cast<uint4*>(host + part * 32 + v * 8) = o;  // the append
-          }
+        for (int q = 0; q < 4; ++q) {
+          const uint4 o = pack8<T>(v + q * 8, 1.f);
+          if (mine) *reinterpret_cast<uint4*>(tile + swz(r, part * 4 + q, kRegKV)) = o;
+          if (append) *reinterpret_cast<uint4*>(host + part * 32 + q * 8) = o;  // the append
         }
       }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->pr_drain);
     }
     // the host rows have landed (loader's cp.async tracked by kv_host)
     wait_or_abort(&bars->kv_host, 0, bars, a.status, kSiteFull);
-    if (grp == 1) {
+    if (hh == 1) {
       // P.V runs in fp16 (P keeps 11 significant bits).  For bf16 inputs the
       // stationary V chunk is converted to fp16 in place, times 2^-k with k the
       // smallest power making max|V| < 2^15 (k = 0 unless V is huge); the
@@ -340,36 +399,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (DT<T>::code == DKV_BF16) {
         float vmax = 0.f;
 #pragma unroll
-        for (int cc = 0; cc < D / 8; ++cc) {
-          const uint4 u = *reinterpret_cast<const uint4*>(vs + swz_off(row, cc));
-          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+        for (int rr = 0; rr < 2; ++rr) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = DT<T>::to_f2(w4[e]);
-            vmax = fmaxf(vmax, fmaxf(fabsf(f.x), fabsf(f.y)));
+          for (int cc = 0; cc < D / 8; ++cc) {
+            const uint4 u = *reinterpret_cast<const uint4*>(vs + swz(rr * 128 + row, cc, kRegKV));
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = DT<T>::to_f2(w4[e]);
+              vmax = fmaxf(vmax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
           }
         }
         for (int off = 16; off > 0; off >>= 1)
           vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
         if (lane == 0) bars->vmax[quarter] = vmax;
-        named_bar_sync(2, 128);
+        warps_sync(&bars->vsync, 0, bars, a.status);
         vmax = fmaxf(fmaxf(bars->vmax[0], bars->vmax[1]), fmaxf(bars->vmax[2], bars->vmax[3]));
         int e2 = 0;
         (void)frexpf(vmax, &e2);  // vmax < 2^e2
         k = (vmax == vmax && e2 > 15) ? e2 - 15 : 0;
         const float sc = exp2f((float)-k);
 #pragma unroll
-        for (int cc = 0; cc < D / 8; ++cc) {
-          uint4* p16 = reinterpret_cast<uint4*>(vs + swz_off(row, cc));
-          const uint4 u = *p16;
-          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-          uint32_t h4[4];
+        for (int rr = 0; rr < 2; ++rr) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = DT<T>::to_f2(w4[e]);
-            h4[e] = tc::pack2<__half>(f.x * sc, f.y * sc);
+          for (int cc = 0; cc < D / 8; ++cc) {
+            uint4* p16 = reinterpret_cast<uint4*>(vs + swz(rr * 128 + row, cc, kRegKV));
+            const uint4 u = *p16;
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+            uint32_t h4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = DT<T>::to_f2(w4[e]);
+              h4[e] = tc::pack2<__half>(f.x * sc, f.y * sc);
+            }
+            *p16 = make_uint4(h4[0], h4[1], h4[2], h4[3]);
           }
-          *p16 = make_uint4(h4[0], h4[1], h4[2], h4[3]);
         }
       }
       if (warp == 6 && lane == 0) a.part_k[(size_t)c * a.B * a.Hkv + bh] = k;
@@ -379,65 +444,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars->kv_ready);
 
-    // (b) this group's Q tiles: softmax, then the output epilogue
+    // (b) the Q tiles: softmax over this half's 128 scores, then the output
+    //     epilogue for this half's D/2 columns
+    (void)hrow;
     const float scale = a.scale_log2;
-    const int s = grp;
-    const uint32_t s_tm = tmem + s * 128 + lane_off;
-    const uint32_t o_tm = tmem + 256 + s * 128 + lane_off;
-    uint8_t* prow = ps + s * Cfg::kP;
-    const bool leader = warp == 2 + 4 * grp && lane == 0;  // issues this group's TMA stores
-    // partials of this unit: block (c, b, kvh) of T*G rows ordered (token, head)
+    const bool leader = warp == 2 && lane == 0;  // issues the TMA stores
     const size_t TG = (size_t)a.T * G;
     const size_t blk = ((size_t)c * a.B + b) * a.Hkv + kvh;
-    for (int i = grp; i < ntiles; i += 2) {
-      const uint32_t ph = (i >> 1) & 1;
-      if (!warp_wait(&bars->s_full[s], ph, bars, a.status, kSiteFull)) break;
+    for (int i = 0; i < ntiles; ++i) {
+      const uint32_t ph = i & 1;
+      if (!warp_wait(&bars->s_full, ph, bars, a.status, kSiteFull)) break;
       tc::fence_after_sync();
       const int t_first = t_lo + i * TQ;
       // every key of the chunk is visible to every row of this tile
       const bool full = nkeys == kC && P + t_first >= k0 + kC - 1;
       const int t = t_first + row / G;
-      const int nvis = min(nkeys, P + t - k0 + 1);
-      // the whole S row in registers: four TMEM loads in flight, one wait
-      uint32_t r[kC];
+      const int nvis = min(nkeys, P + t - k0 + 1) - hh * 128;  // visible keys in this half
+      uint32_t r[128];
 #pragma unroll
-      for (int part = 0; part < kC / 32; ++part)
-        tc::tmem_ld32(s_tm + part * 32, *reinterpret_cast<uint32_t(*)[32]>(r + part * 32));
+      for (int part = 0; part < 4; ++part)
+        tc::tmem_ld32(tmem + lane_off + kTmS + hh * 128 + part * 32,
+                      *reinterpret_cast<uint32_t(*)[32]>(r + part * 32));
       tc::tmem_wait_ld();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_empty[s]);  // S may be overwritten by tile i + 2
-      // row max of the visible raw scores (eight independent chains)
+      if (lane == 0) mbar_arrive(&bars->s_empty);  // S may be overwritten by tile i + 1
       float m8[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) m8[q] = -INFINITY;
       if (full) {
 #pragma unroll
-        for (int j = 0; j < kC; ++j) m8[j % 8] = fmaxf(m8[j % 8], __uint_as_float(r[j]));
+        for (int j = 0; j < 128; ++j) m8[j % 8] = fmaxf(m8[j % 8], __uint_as_float(r[j]));
       } else {
 #pragma unroll
-        for (int j = 0; j < kC; ++j)
+        for (int j = 0; j < 128; ++j)
           if (j < nvis) m8[j % 8] = fmaxf(m8[j % 8], __uint_as_float(r[j]));
       }
-      const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      const float mx = mraw * scale;
-      // P = 2^(s*scale - m) in fp16; l sums the rounded weights so the P.V
-      // product is normalised by exactly the weights it used.
-      if (!warp_wait(&bars->p_empty[s], ph ^ 1, bars, a.status, kSiteEmpty)) break;
-      // the P buffer also staged the previous tile's output: its TMA store
-      // must have finished reading it
-      if (i >= 2) {
-        if (leader) tc::bulk_wait_read_all();
-        named_bar_sync(3 + grp, 128);
-      }
+      bars->xmax[hh][row] = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                  fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      if (!warps_sync(&bars->xsync[0], ph, bars, a.status)) break;
+      const float mx = fmaxf(bars->xmax[0][row], bars->xmax[1][row]) * scale;
+      // P = 2^(s*scale - m) in fp16 into TMEM; l sums the rounded weights so
+      // the P.V product is normalised by exactly the weights it used.
+      if (!warp_wait(&bars->p_empty, ph ^ 1, bars, a.status, kSiteEmpty)) break;
       float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int cc = 0; cc < kC / 8; ++cc) {
-        uint32_t w[4];
+      for (int part = 0; part < 2; ++part) {
+        uint32_t w[32];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = cc * 8 + 2 * e;
+        for (int e = 0; e < 32; ++e) {
+          const int j = part * 64 + 2 * e;
           float p0 = tc::ex2_approx(fmaf(__uint_as_float(r[j]), scale, -mx));
           float p1 = tc::ex2_approx(fmaf(__uint_as_float(r[j + 1]), scale, -mx));
           if (!full) {
@@ -446,38 +502,46 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           w[e] = tc::pack2<__half>(p0, p1);
           const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-          l8[2 * e] += back.x;
-          l8[2 * e + 1] += back.y;
+          l8[(2 * e) % 8] += back.x;
+          l8[(2 * e + 1) % 8] += back.y;
         }
-        *reinterpret_cast<uint4*>(prow + swz_off(row, cc)) = make_uint4(w[0], w[1], w[2], w[3]);
+        tc::tmem_st32(tmem + lane_off + kTmP + hh * 64 + part * 32, w);
       }
-      const float l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
-      tc::fence_proxy_async_smem();
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[s]);  // P is ready for the P.V MMA
-      // epilogue of this tile: O / l in fp16 staged in the (consumed) P buffer
-      // and written with TMA stores; the base-2 lse with plain stores.  Both
-      // land tile-contiguous: block (c, b, kvh), rows (t, g).
-      if (!warp_wait(&bars->o_full[s], ph, bars, a.status, kSiteFull)) break;
+      if (lane == 0) mbar_arrive(&bars->p_full);  // P is ready for the P.V MMA
+      bars->xl[hh][row] =
+          ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+      // epilogue: O / l in fp16 staged in shared memory, written with TMA
+      // stores; the base-2 lse with plain stores.  Both land tile-contiguous:
+      // block (c, b, kvh), rows (t, g).
+      if (!warp_wait(&bars->o_full, ph, bars, a.status, kSiteFull)) break;
       tc::fence_after_sync();
-      const float inv = 1.f / l;
+      if (leader) tc::bulk_wait_read_all();  // the previous tile's stores left the staging
+      if (!warps_sync(&bars->xsync[1], ph, bars, a.status)) break;
+      const float l = bars->xl[0][row] + bars->xl[1][row];
+      constexpr int DH = D / 2;  // output columns per half
 #pragma unroll
-      for (int part = 0; part < D / 32; ++part)
-        tc::tmem_ld32(o_tm + part * 32, *reinterpret_cast<uint32_t(*)[32]>(r + part * 32));
+      for (int part = 0; part < DH / 32; ++part)
+        tc::tmem_ld32(tmem + lane_off + kTmO + hh * DH + part * 32,
+                      *reinterpret_cast<uint32_t(*)[32]>(r + part * 32));
       tc::tmem_wait_ld();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->o_empty[s]);  // O may be overwritten by tile i + 2
+      if (lane == 0) mbar_arrive(&bars->o_empty);  // O may be overwritten by tile i + 1
+      const float inv = 1.f / l;
 #pragma unroll
-      for (int v = 0; v < D / 8; ++v)
-        *reinterpret_cast<uint4*>(prow + swz_off(row, v)) = pack8<__half>(r + v * 8, inv);
-      if (t < a.T) a.part_lse[blk * TG + (size_t)t * G + row % G] = mx + log2f(l);
+      for (int q = 0; q < DH / 8; ++q)
+        *reinterpret_cast<uint4*>(os + swz(row, hh * (DH / 8) + q, kRegQ)) =
+            pack8<__half>(r + q * 8, inv);
+      if (hh == 0 && t < a.T) a.part_lse[blk * TG + (size_t)t * G + row % G] = mx + log2f(l);
       tc::fence_proxy_async_smem();
-      named_bar_sync(3 + grp, 128);
+      if (!warps_sync(&bars->xsync[2], ph, bars, a.status)) break;
       if (leader) {
 #pragma unroll
         for (int rg = 0; rg < DR; ++rg)
-          tc::tma_store_3d(&map_po, rg * 64, t_first * G, (int)blk, prow + rg * kRegion);
+          tc::tma_store_3d(&map_po, rg * 64, t_first * G, (int)blk, os + rg * kRegQ);
         tc::bulk_commit();
       }
     }
@@ -547,7 +611,7 @@ cudaError_t launch_t(const TcArgs& args, const CUtensorMap& mq, const CUtensorMa
                      const KernelTimer& timer) {
   auto k = prefill_tc_kernel<T, D, G>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       TcCfg<D>::kSmem);
+                                       smem_request<D>());
   if (e != cudaSuccess) return e;
   CUtensorMap mpo;
   if (!make_tmap_partial(&mpo, args.part_o, D, (uint64_t)args.T * G,
@@ -555,7 +619,7 @@ cudaError_t launch_t(const TcArgs& args, const CUtensorMap& mq, const CUtensorMa
     return cudaErrorInvalidValue;
   const int units = args.B * args.Hkv * args.nchunks;
   timer.before(s);
-  k<<<units, kThreads, TcCfg<D>::kSmem, s>>>(mq, mx, mk, mv, mpo, args);
+  k<<<units, kThreads, smem_request<D>(), s>>>(mq, mx, mk, mv, mpo, args);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   timer.after(s);
   LenArray len;
