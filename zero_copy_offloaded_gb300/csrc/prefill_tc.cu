@@ -451,11 +451,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = warp == 2 && lane == 0;  // issues the TMA stores
     const size_t TG = (size_t)a.T * G;
     const size_t blk = ((size_t)c * a.B + b) * a.Hkv + kvh;
-    for (int i = 0; i < ntiles; ++i) {
-      const uint32_t ph = i & 1;
-      if (!warp_wait(&bars->s_full, ph, bars, a.status, kSiteFull)) break;
+    // softmax(j): S -> P (TMEM) for tile j; returns this half's row sum and
+    // the row max (scaled) in registers for the epilogue of tile j.  Its
+    // max-exchange rendezvous also publishes the previous tile's half sums
+    // (l_prev) and, through the leader, frees the output staging for the
+    // epilogue of tile j - 1 that follows it.
+    auto softmax = [&](int j, float l_prev, float& l_out, float& m_out) -> bool {
+      const uint32_t ph = j & 1;
+      if (!warp_wait(&bars->s_full, ph, bars, a.status, kSiteFull)) return false;
       tc::fence_after_sync();
-      const int t_first = t_lo + i * TQ;
+      const int t_first = t_lo + j * TQ;
       // every key of the chunk is visible to every row of this tile
       const bool full = nkeys == kC && P + t_first >= k0 + kC - 1;
       const int t = t_first + row / G;
@@ -468,42 +473,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tmem_wait_ld();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_empty);  // S may be overwritten by tile i + 1
+      if (lane == 0) mbar_arrive(&bars->s_empty);  // S may be overwritten by tile j + 1
       float m8[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) m8[q] = -INFINITY;
       if (full) {
 #pragma unroll
-        for (int j = 0; j < 128; ++j) m8[j % 8] = fmaxf(m8[j % 8], __uint_as_float(r[j]));
+        for (int k2 = 0; k2 < 128; ++k2) m8[k2 % 8] = fmaxf(m8[k2 % 8], __uint_as_float(r[k2]));
       } else {
 #pragma unroll
-        for (int j = 0; j < 128; ++j)
-          if (j < nvis) m8[j % 8] = fmaxf(m8[j % 8], __uint_as_float(r[j]));
+        for (int k2 = 0; k2 < 128; ++k2)
+          if (k2 < nvis) m8[k2 % 8] = fmaxf(m8[k2 % 8], __uint_as_float(r[k2]));
       }
       bars->xmax[hh][row] = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      if (!warps_sync(&bars->xsync[0], ph, bars, a.status)) break;
+      if (j > 0) {
+        bars->xl[hh][row] = l_prev;
+        if (leader) tc::bulk_wait_read_all();  // tile j-2's stores left the staging
+      }
+      if (!warps_sync(&bars->xsync[0], ph, bars, a.status)) return false;
       const float mx = fmaxf(bars->xmax[0][row], bars->xmax[1][row]) * scale;
-      // P = 2^(s*scale - m) in fp16 into TMEM; l sums the rounded weights so
-      // the P.V product is normalised by exactly the weights it used.
-      if (!warp_wait(&bars->p_empty, ph ^ 1, bars, a.status, kSiteEmpty)) break;
+      // P = 2^(s*scale - m) in fp16 into TMEM (l sums the weights before the
+      // rounding: the normalisation then differs from the rounded weights'
+      // sum by at most 2^-12 relative).  P of tile j - 1 must have been
+      // consumed by its P.V first.
+      if (!warp_wait(&bars->p_empty, ph ^ 1, bars, a.status, kSiteEmpty)) return false;
       float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         uint32_t w[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const int j = part * 64 + 2 * e;
-          float p0 = tc::ex2_approx(fmaf(__uint_as_float(r[j]), scale, -mx));
-          float p1 = tc::ex2_approx(fmaf(__uint_as_float(r[j + 1]), scale, -mx));
+          const int k2 = part * 64 + 2 * e;
+          float p0 = tc::ex2_approx(fmaf(__uint_as_float(r[k2]), scale, -mx));
+          float p1 = tc::ex2_approx(fmaf(__uint_as_float(r[k2 + 1]), scale, -mx));
           if (!full) {
-            p0 = j < nvis ? p0 : 0.f;
-            p1 = j + 1 < nvis ? p1 : 0.f;
+            p0 = k2 < nvis ? p0 : 0.f;
+            p1 = k2 + 1 < nvis ? p1 : 0.f;
           }
           w[e] = tc::pack2<__half>(p0, p1);
-          const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-          l8[(2 * e) % 8] += back.x;
-          l8[(2 * e + 1) % 8] += back.y;
+          l8[(2 * e) % 8] += p0;
+          l8[(2 * e + 1) % 8] += p1;
         }
         tc::tmem_st32(tmem + lane_off + kTmP + hh * 64 + part * 32, w);
       }
@@ -511,17 +521,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->p_full);  // P is ready for the P.V MMA
-      bars->xl[hh][row] =
-          ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
-      // epilogue: O / l in fp16 staged in shared memory, written with TMA
-      // stores; the base-2 lse with plain stores.  Both land tile-contiguous:
-      // block (c, b, kvh), rows (t, g).
-      if (!warp_wait(&bars->o_full, ph, bars, a.status, kSiteFull)) break;
+      l_out = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+      m_out = mx;
+      return true;
+    };
+    // epilogue(j): O / l in fp16 staged in shared memory, written with TMA
+    // stores; the base-2 lse with plain stores.  Both land tile-contiguous:
+    // block (c, b, kvh), rows (t, g).
+    auto epilogue = [&](int j, float l_half, float mx, bool last) -> bool {
+      const uint32_t ph = j & 1;
+      const int t_first = t_lo + j * TQ;
+      const int t = t_first + row / G;
+      if (!warp_wait(&bars->o_full, ph, bars, a.status, kSiteFull)) return false;
       tc::fence_after_sync();
-      if (leader) tc::bulk_wait_read_all();  // the previous tile's stores left the staging
-      if (!warps_sync(&bars->xsync[1], ph, bars, a.status)) break;
+      if (last) {  // no later softmax published the half sums: rendezvous here
+        bars->xl[hh][row] = l_half;
+        if (leader) tc::bulk_wait_read_all();
+        if (!warps_sync(&bars->xsync[1], 0, bars, a.status)) return false;
+      }
       const float l = bars->xl[0][row] + bars->xl[1][row];
       constexpr int DH = D / 2;  // output columns per half
+      uint32_t r[DH];
 #pragma unroll
       for (int part = 0; part < DH / 32; ++part)
         tc::tmem_ld32(tmem + lane_off + kTmO + hh * DH + part * 32,
@@ -529,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tmem_wait_ld();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->o_empty);  // O may be overwritten by tile i + 1
+      if (lane == 0) mbar_arrive(&bars->o_empty);  // O may be overwritten by tile j + 1
       const float inv = 1.f / l;
 #pragma unroll
       for (int q = 0; q < DH / 8; ++q)
@@ -537,12 +557,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             pack8<__half>(r + q * 8, inv);
       if (hh == 0 && t < a.T) a.part_lse[blk * TG + (size_t)t * G + row % G] = mx + log2f(l);
       tc::fence_proxy_async_smem();
-      if (!warps_sync(&bars->xsync[2], ph, bars, a.status)) break;
+      if (!warps_sync(&bars->xsync[2], ph, bars, a.status)) return false;
       if (leader) {
 #pragma unroll
         for (int rg = 0; rg < DR; ++rg)
           tc::tma_store_3d(&map_po, rg * 64, t_first * G, (int)blk, os + rg * kRegQ);
         tc::bulk_commit();
+      }
+      return true;
+    };
+    // softmax of tile i+1 runs before the epilogue of tile i, so the P.V of
+    // tile i proceeds on the tensor cores meanwhile
+    float l_cur = 0.f, m_cur = 0.f;
+    if (softmax(0, 0.f, l_cur, m_cur)) {
+      for (int i = 0; i < ntiles; ++i) {
+        float l_next = 0.f, m_next = 0.f;
+        const bool last = i + 1 == ntiles;
+        if (!last && !softmax(i + 1, l_cur, l_next, m_next)) break;
+        if (!epilogue(i, l_cur, m_cur, last)) break;
+        l_cur = l_next;
+        m_cur = m_next;
       }
     }
     if (leader) tc::bulk_wait_all();
