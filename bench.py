@@ -265,9 +265,10 @@ def main():
     import torch
     import zero_copy_offloaded_gb300 as dkv
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from zero_copy_offloaded_gb300 import ranks as rk
+
+    rks = rk.Ranks.from_env()
+    world, rank, local = rks.world, rks.rank, rks.local
     torch.cuda.set_device(local)
     dist = None
     if world > 1:
@@ -277,16 +278,11 @@ def main():
     stream = torch.cuda.current_stream()
 
     def barrier():
-        if dist:
-            dist.barrier()
+        rk.barrier(dist)
         torch.cuda.synchronize()
 
     def max_over_ranks(v):
-        if not dist:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return rk.max_over_ranks(v, dist, dev)
 
     pk = peaks()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -356,7 +352,7 @@ def main():
     cache.sync(stream)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     tot_s = max_over_ranks(sum(step_ms) / 1e3)
-    value = w.B * args.steps * world / tot_s
+    value = rk.job_rate(w.B * args.steps, world, tot_s)
     fused_ms = statistics.mean(kern_ms)
 
     # ------------------------------------------------ link / HBM probes
@@ -419,7 +415,7 @@ def main():
         b.synchronize()
         if i >= args.warmup:
             e2e_ms.append(a.elapsed_time(b))
-    e2e_val = w.B * len(e2e_ms) * world / max_over_ranks(sum(e2e_ms) / 1e3)
+    e2e_val = rk.job_rate(w.B * len(e2e_ms), world, max_over_ranks(sum(e2e_ms) / 1e3))
 
     extras = {}
     if not args.no_extras:
