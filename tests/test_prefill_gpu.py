@@ -12,16 +12,19 @@ import pytest
 
 from zero_copy_offloaded_gb300 import workloads as wl
 
-from .helpers import Case, assert_close, assert_projection_close, out_f64
+from .helpers import (Case, assert_close, assert_close_beyond_rounding, assert_projection_close,
+                      out_f64)
 
 pytestmark = pytest.mark.gpu
 
 
-def check_prefill(case: Case, out, ref, label="", rows=None):
+def check_prefill(case: Case, out, ref, label="", rows=None, beyond_rounding=False):
     w = case.w
     T = out.shape[1]
     got = out_f64(out, w.dtype).reshape(w.B, T, w.Hq, w.D)
-    if rows is None:
+    if beyond_rounding:
+        res = assert_close_beyond_rounding(got, ref["out"], w.dtype, label)
+    elif rows is None:
         res = assert_close(got, ref["out"], label)
     else:
         g = np.stack([got[b, t] for (b, t) in rows])
@@ -50,6 +53,43 @@ def test_prefill_shapes(dtype, D, Hq, Hkv, P, T):
     try:
         out = case.run_prefill()
         check_prefill(case, out, case.oracle(), f"{dtype} D{D} G{Hq // Hkv} P{P} T{T}")
+    finally:
+        case.free()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_prefill_spiky_keys(dtype):
+    """5 % of the cached key rows scaled by 8 (the long-context recipe, denser).
+
+    The fused kernel forms a row's weights for the first 128 keys of a chunk
+    against their own max and rescales them only when the second 128 keys'
+    max is larger by more than a factor 2^8 in weight; spikes make that common, so both ways
+    through the softmax are compared with the oracle.  The fraction of (query
+    row, prefix chunk) pairs that take the rescale is computed here from the
+    oracle's q, so the case is known to exercise it."""
+    w = wl.Workload("t", "prefill", B=2, H=128, Hq=8, Hkv=2, D=128, P=700, T=90, dtype=dtype,
+                    kv_dist="uniform2" if dtype == "fp16" else "normal", spike_frac=0.05,
+                    seed=11)
+    case = Case(w, s_max=w.P + w.T + 3)
+    try:
+        out = case.run_prefill()
+        ref = case.oracle()
+        # attention concentrates on single value rows, so outputs reach |o| >= 4
+        # where bf16's own rounding exceeds the flat max-abs bar
+        check_prefill(case, out, ref, f"spiky {dtype}", beyond_rounding=True)
+        q = wl.bits_to_f32(ref["q"], dtype).astype(np.float64)  # [B,T,Hq,D]
+        K = wl.bits_to_f32(case.k0, dtype).astype(np.float64)  # [B,Hkv,s_max,D]
+        G = w.Hq // w.Hkv
+        hits = total = 0
+        for b in range(w.B):
+            for h in range(w.Hq):
+                s = q[b, :, h] @ K[b, h // G, :512].T / np.sqrt(w.D) * np.log2(np.e)
+                for c in range(2):  # chunks wholly in the prefix: every query sees them
+                    m0 = s[:, c * 256:c * 256 + 128].max(axis=1)
+                    m1 = s[:, c * 256 + 128:c * 256 + 256].max(axis=1)
+                    hits += int(np.sum(m1 > m0 + 8))
+                    total += m0.size
+        assert hits / total > 0.05, f"rescale taken by only {hits}/{total} rows"
     finally:
         case.free()
 

@@ -198,7 +198,7 @@ bool make_tmap_partial(CUtensorMap* map, void* base, int D, uint64_t rows, uint6
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)D, rows, blocks};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, rows * D * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, 32, 1};  // one warp's 32 rows
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

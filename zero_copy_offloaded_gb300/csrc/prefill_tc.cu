@@ -83,7 +83,9 @@ constexpr int smem_request() {
 struct Bars {
   uint64_t q_full[2], q_empty[2], s_full, s_empty, p_full, p_empty, o_full, o_empty, kv_host,
       kv_ready, pr_full[2], pr_empty[2], pr_done, pr_drain;
-  uint64_t xsync[3];  // softmax-warp rendezvous points of a tile (8 warps each)
+  // rendezvous of the two warps sharing a TMEM lane quarter (halves of the
+  // same rows): max exchange, last-tile sum exchange, shared staging (D = 64)
+  uint64_t xpair[3][4];
   uint64_t vsync;     // rendezvous of the four warps converting V
   uint32_t tmem_base;
   volatile int abort;
@@ -207,7 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->kv_ready, 8);
     mbar_init(&bars->pr_done, 1);
     mbar_init(&bars->pr_drain, 8);
-    for (int i = 0; i < 3; ++i) mbar_init(&bars->xsync[i], 8);
+    for (int i = 0; i < 3; ++i)
+      for (int q = 0; q < 4; ++q) mbar_init(&bars->xpair[i][q], 2);
     mbar_init(&bars->vsync, 4);
     bars->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -448,14 +451,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     //     epilogue for this half's D/2 columns
     (void)hrow;
     const float scale = a.scale_log2;
-    const bool leader = warp == 2 && lane == 0;  // issues the TMA stores
+    // With D = 128 each warp stores its own 64 output columns of its 32 rows;
+    // with D = 64 the two halves share one 128-byte row and the half-0 warp
+    // stores it.
+    constexpr bool kOwnStore = DR == 2;
+    const bool storer = lane == 0 && (kOwnStore || hh == 0);
     const size_t TG = (size_t)a.T * G;
     const size_t blk = ((size_t)c * a.B + b) * a.Hkv + kvh;
     // softmax(j): S -> P (TMEM) for tile j; returns this half's row sum and
     // the row max (scaled) in registers for the epilogue of tile j.  Its
-    // max-exchange rendezvous also publishes the previous tile's half sums
-    // (l_prev) and, through the leader, frees the output staging for the
-    // epilogue of tile j - 1 that follows it.
+    // max-exchange rendezvous with the partner warp also publishes the
+    // previous tile's half sums (l_prev) and, through the storer, frees the
+    // output staging for the epilogue of tile j - 1 that follows it.
     auto softmax = [&](int j, float l_prev, float& l_out, float& m_out) -> bool {
       const uint32_t ph = j & 1;
       if (!warp_wait(&bars->s_full, ph, bars, a.status, kSiteFull)) return false;
@@ -489,34 +496,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       if (j > 0) {
         bars->xl[hh][row] = l_prev;
-        if (leader) tc::bulk_wait_read_all();  // tile j-2's stores left the staging
+        if (storer) tc::bulk_wait_read_all();  // tile j-2's stores left the staging
       }
-      if (!warps_sync(&bars->xsync[0], ph, bars, a.status)) return false;
+      if (!warps_sync(&bars->xpair[0][quarter], ph, bars, a.status)) return false;
       const float mx = fmaxf(bars->xmax[0][row], bars->xmax[1][row]) * scale;
-      // P = 2^(s*scale - m) in fp16 into TMEM (l sums the weights before the
-      // rounding: the normalisation then differs from the rounded weights'
-      // sum by at most 2^-12 relative).  P of tile j - 1 must have been
-      // consumed by its P.V first.
-      if (!warp_wait(&bars->p_empty, ph ^ 1, bars, a.status, kSiteEmpty)) return false;
+      // P = 2^(s*scale - m) in fp16 (l sums the weights before the rounding:
+      // the normalisation then differs from the rounded weights' sum by at
+      // most 2^-12 relative).  The weights are formed in registers while the
+      // P.V of tile j - 1 still reads the previous P from TMEM; only the
+      // stores into TMEM wait for it.
       float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      uint32_t w[64];
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        uint32_t w[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int k2 = part * 64 + 2 * e;
-          float p0 = tc::ex2_approx(fmaf(__uint_as_float(r[k2]), scale, -mx));
-          float p1 = tc::ex2_approx(fmaf(__uint_as_float(r[k2 + 1]), scale, -mx));
-          if (!full) {
-            p0 = k2 < nvis ? p0 : 0.f;
-            p1 = k2 + 1 < nvis ? p1 : 0.f;
-          }
-          w[e] = tc::pack2<__half>(p0, p1);
-          l8[(2 * e) % 8] += p0;
-          l8[(2 * e + 1) % 8] += p1;
+      for (int e = 0; e < 64; ++e) {
+        const int k2 = 2 * e;
+        float p0 = tc::ex2_approx(fmaf(__uint_as_float(r[k2]), scale, -mx));
+        float p1 = tc::ex2_approx(fmaf(__uint_as_float(r[k2 + 1]), scale, -mx));
+        if (!full) {
+          p0 = k2 < nvis ? p0 : 0.f;
+          p1 = k2 + 1 < nvis ? p1 : 0.f;
         }
-        tc::tmem_st32(tmem + lane_off + kTmP + hh * 64 + part * 32, w);
+        w[e] = tc::pack2<__half>(p0, p1);
+        l8[(2 * e) % 8] += p0;
+        l8[(2 * e + 1) % 8] += p1;
       }
+      if (!warp_wait(&bars->p_empty, ph ^ 1, bars, a.status, kSiteEmpty)) return false;
+      tc::tmem_st32(tmem + lane_off + kTmP + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(w));
+      tc::tmem_st32(tmem + lane_off + kTmP + hh * 64 + 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(w + 32));
       tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
@@ -536,8 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_after_sync();
       if (last) {  // no later softmax published the half sums: rendezvous here
         bars->xl[hh][row] = l_half;
-        if (leader) tc::bulk_wait_read_all();
-        if (!warps_sync(&bars->xsync[1], 0, bars, a.status)) return false;
+        if (storer) tc::bulk_wait_read_all();
+        if (!warps_sync(&bars->xpair[1][quarter], 0, bars, a.status)) return false;
       }
       const float l = bars->xl[0][row] + bars->xl[1][row];
       constexpr int DH = D / 2;  // output columns per half
@@ -557,11 +564,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             pack8<__half>(r + q * 8, inv);
       if (hh == 0 && t < a.T) a.part_lse[blk * TG + (size_t)t * G + row % G] = mx + log2f(l);
       tc::fence_proxy_async_smem();
-      if (!warps_sync(&bars->xsync[2], ph, bars, a.status)) return false;
-      if (leader) {
-#pragma unroll
-        for (int rg = 0; rg < DR; ++rg)
-          tc::tma_store_3d(&map_po, rg * 64, t_first * G, (int)blk, os + rg * kRegQ);
+      const int row0 = t_first * G + quarter * 32;  // rows past T*G are clipped by the store
+      if constexpr (!kOwnStore) {
+        if (!warps_sync(&bars->xpair[2][quarter], ph, bars, a.status)) return false;
+      } else {
+        __syncwarp();
+      }
+      if (storer && row0 < (int)TG) {
+        const int rg = kOwnStore ? hh : 0;
+        tc::tma_store_3d(&map_po, rg * 64, row0, (int)blk, os + rg * kRegQ + quarter * 32 * 128);
         tc::bulk_commit();
       }
       return true;
@@ -579,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_cur = m_next;
       }
     }
-    if (leader) tc::bulk_wait_all();
+    if (storer) tc::bulk_wait_all();
   }
 
   tc::fence_before_sync();
