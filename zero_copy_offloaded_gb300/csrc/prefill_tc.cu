@@ -86,6 +86,9 @@ struct Bars {
   // rendezvous of the two warps sharing a TMEM lane quarter (halves of the
   // same rows): max exchange, last-tile sum exchange, shared staging (D = 64)
   uint64_t xpair[3][4];
+  // the pair has read the exchange slots (xmax, xl) of a step: one arrival
+  // per warp, waited on only before the slots are written again
+  uint64_t xfree[4];
   uint64_t vsync;     // rendezvous of the four warps converting V
   uint32_t tmem_base;
   volatile int abort;
@@ -103,7 +106,8 @@ struct TcArgs {
   float* part_lse;  // [nchunks, B, Hkv, T, G]
   int* part_k;      // [nchunks, B*Hkv]
   DeviceStatus* status;
-  int B, T, H, Hq, Hkv, S_max, nchunks;
+  int B, T, H, Hq, Hkv, nchunks;
+  CacheLayout lay;  // rows of the caches (dense or paged)
   float scale_log2;
   int len[kMaxBatch];
 };
@@ -211,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->pr_drain, 8);
     for (int i = 0; i < 3; ++i)
       for (int q = 0; q < 4; ++q) mbar_init(&bars->xpair[i][q], 2);
+    for (int q = 0; q < 4; ++q) mbar_init(&bars->xfree[q], 2);
     mbar_init(&bars->vsync, 4);
     bars->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -221,21 +226,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
   const int nk_proj = (a.H + 63) / 64;  // TMA zero-fills past H
-  const size_t head_off = ((size_t)b * a.Hkv + kvh) * a.S_max * D;
 
   if (warp == 0) {
     // ================================================================ loader
     // (a) cached rows of the chunk: host -> shared, 16-byte cp.async, swizzled.
     {
-      const T* kg = static_cast<const T*>(a.k_read) + head_off + (size_t)k0 * D;
-      const T* vg = static_cast<const T*>(a.v_read) + head_off + (size_t)k0 * D;
+      const T* kg = static_cast<const T*>(a.k_read);
+      const T* vg = static_cast<const T*>(a.v_read);
       constexpr int CPR = D / 8;  // 16-byte chunks per row
       const int rows = has_new ? nhost : kC;  // zero-fill the tail when nothing is projected
       for (int i = lane; i < rows * CPR; i += 32) {
         const int r = i / CPR, cc = i % CPR;
         const int off = swz(r, cc, kRegKV);
         const bool ok = r < nhost;
-        const size_t src = ok ? (size_t)r * D + cc * 8 : 0;
+        const size_t src = ok ? a.lay.row(b, kvh, k0 + r, D) + cc * 8 : 0;
         cp_async16(ks + off, kg + src, ok ? 16 : 0);
         cp_async16(vs + off, vg + src, ok ? 16 : 0);
       }
@@ -374,7 +378,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool mine = r >= nhost;            // this row is a new key projected here
       const bool append = mine && key < S;
       uint8_t* tile = hh ? vs : ks;
-      T* host = static_cast<T*>(hh ? a.v_host : a.k_host) + head_off + (size_t)key * D;
+      // (the row is looked up only where it exists: key < S)
+      T* host = append ? static_cast<T*>(hh ? a.v_host : a.k_host) + a.lay.row(b, kvh, key, D)
+                       : nullptr;
 #pragma unroll 1
       for (int part = 0; part < D / 32; ++part) {
         uint32_t v[32];
@@ -492,6 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k2 = 0; k2 < 128; ++k2)
           if (k2 < nvis) m8[k2 % 8] = fmaxf(m8[k2 % 8], __uint_as_float(r[k2]));
       }
+      // the partner has read the slots of the previous step (its xmax of
+      // tile j - 1 and xl of tile j - 2) before they are overwritten
+      if (j > 0 && !warp_wait(&bars->xfree[quarter], (j - 1) & 1, bars, a.status, kSiteEmpty))
+        return false;
       bars->xmax[hh][row] = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       if (j > 0) {
@@ -500,6 +510,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!warps_sync(&bars->xpair[0][quarter], ph, bars, a.status)) return false;
       const float mx = fmaxf(bars->xmax[0][row], bars->xmax[1][row]) * scale;
+      if (j == 0) {  // step 0 of the exchange slots is read
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->xfree[quarter]);
+      }
       // P = 2^(s*scale - m) in fp16 (l sums the weights before the rounding:
       // the normalisation then differs from the rounded weights' sum by at
       // most 2^-12 relative).  The weights are formed in registers while the
@@ -542,11 +556,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(&bars->o_full, ph, bars, a.status, kSiteFull)) return false;
       tc::fence_after_sync();
       if (last) {  // no later softmax published the half sums: rendezvous here
+        if (!warp_wait(&bars->xfree[quarter], j & 1, bars, a.status, kSiteEmpty)) return false;
         bars->xl[hh][row] = l_half;
         if (storer) tc::bulk_wait_read_all();
         if (!warps_sync(&bars->xpair[1][quarter], 0, bars, a.status)) return false;
       }
       const float l = bars->xl[0][row] + bars->xl[1][row];
+      if (!last) {  // step j + 1 of the exchange slots is read
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->xfree[quarter]);
+      }
       constexpr int DH = D / 2;  // output columns per half
       uint32_t r[DH];
 #pragma unroll
@@ -705,7 +724,7 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, const void* wq,
   TcArgs a;
   a.k_read = p.k_read; a.v_read = p.v_read; a.k_host = p.k_host; a.v_host = p.v_host;
   a.part_o = p.part_o; a.part_lse = p.part_lse; a.part_k = p.part_k; a.status = p.status;
-  a.B = p.B; a.T = p.T; a.H = p.H; a.Hq = p.Hq; a.Hkv = p.Hkv; a.S_max = p.S_max;
+  a.B = p.B; a.T = p.T; a.H = p.H; a.Hq = p.Hq; a.Hkv = p.Hkv; a.lay = p.lay;
   a.nchunks = p.nchunks; a.scale_log2 = p.scale_log2;
   for (int i = 0; i < kMaxBatch; ++i) a.len[i] = p.len[i];
 #define DKV_TC(TT, DD, GG) \
