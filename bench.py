@@ -57,6 +57,50 @@ def parse():
     return ap.parse_args()
 
 
+def bench_paged_decode(w, page_tokens, dkv, torch, dev, stream, flush, link_rd, steps):
+    """The decode workload on a paged cache: pages of `page_tokens` rows, each
+    sequence's pages drawn by a seeded permutation of the pool (no two
+    consecutive logical pages adjacent), the same inputs as the dense run."""
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+    npg = -(-w.S_max // page_tokens)
+    table = np.random.default_rng(w.seed).permutation(w.B * npg).reshape(w.B, npg)
+    table = table.astype(np.int32)
+    cache = dkv.PagedKVCache(w.B, w.Hkv, w.D, page_tokens, w.B * npg, npg, w.dtype)
+    cache.set_page_table(table)
+    full = w.P // page_tokens  # whole pages of prefix; the rest of the last page below
+    for b in range(w.B):
+        for h in range(w.Hkv):
+            kk, vv = wl.cache_slice(w, b, h)
+            for pool, rows in ((cache.k_host, kk), (cache.v_host, vv)):
+                pool[table[b, :full], h] = rows[:full * page_tokens].reshape(full, page_tokens, w.D)
+                tail = w.P - full * page_tokens
+                if tail:
+                    pool[table[b, full], h, :tail] = rows[full * page_tokens:]
+    dense = wl.make_dense(w)
+    x, wq, wk, wv = (torch.from_numpy(dense[k].view(np.int16)).view(tdt).to(dev)
+                     for k in ("x", "wq", "wk", "wv"))
+    x = x.reshape(w.B, 1, w.H)
+    out = torch.empty((w.B, 1, w.Hq, w.D), dtype=tdt, device=dev)
+    lens = np.full(w.B, w.P, np.int32)
+    dkv.dkv_cache_kernel_timing(cache.h, True)
+
+    def step():
+        cache.set_lengths(lens)
+        cache.decode(x, wq, wk, wv, w.Hq, out, stream)
+    for _ in range(3):
+        step()
+    ms, kern = [], []
+    for _ in range(max(steps, 5)):
+        ms.append(_time_once(torch, stream, flush, step))
+        kern.append(dkv.dkv_cache_last_kernel_ms(cache.h))
+    cache.free()
+    step_ms, kern_ms = statistics.median(ms), statistics.median(kern)
+    gbs = w.host_read_bytes() / (kern_ms * 1e-3) / 1e9
+    return {"workload": w.name, "page_tokens": page_tokens, "pages": int(w.B * npg),
+            "step_ms": step_ms, "tok_s": w.B / (step_ms * 1e-3), "fused_kernel_ms": kern_ms,
+            "host_link_gbs": gbs, "frac_of_link": gbs / link_rd}
+
+
 def sweep(args, dkv, torch, dev, stream, flush, pk):
     """All workloads, one JSON line each (secondary measurements, not the headline)."""
     # link denominators over a 1 GiB mapped buffer
@@ -121,6 +165,10 @@ def sweep(args, dkv, torch, dev, stream, flush, pk):
             "fused_kernel_ms": kern, "host_link_gbs": hb / (kern * 1e-3) / 1e9,
             "frac_of_link": hb / (kern * 1e-3) / 1e9 / link_rd,
             "naive_zero_copy_ms": naive, "copy_to_hbm_then_attend_ms": staged_ms}), flush=True)
+    for name in ("llama8b_decode", "longctx_b1_s128k"):
+        res = bench_paged_decode(wl.WORKLOADS[name], 16, dkv, torch, dev, stream, flush, link_rd,
+                                 args.steps)
+        print(json.dumps({"sweep": name + "_paged16", "phase": "decode", **res}), flush=True)
     for name, w in wl.WORKLOADS.items():
         if w.phase != "prefill":
             continue
@@ -441,6 +489,10 @@ def main():
         extras["prefill"] = bench_prefill(args, dkv, torch, dev, stream, flush, pk, link_rd,
                                           link_wr, hbm_rd)
     cache.free()
+    if not args.no_extras:
+        # the same decode on a paged cache (16-token pages, shuffled page table)
+        extras["paged_decode"] = bench_paged_decode(w, 16, dkv, torch, dev, stream, flush,
+                                                    link_rd, args.steps)
 
     cpu = None
     if rank == 0 and not args.no_extras:

@@ -69,6 +69,9 @@ typedef struct {
     size_t device_workspace_bytes; /* library-owned HBM for q, fresh K/V, partials */
     size_t device_staging_bytes;   /* HBM copies of the cache: always 0 */
     int batch, n_kv_heads, head_dim, max_tokens, dtype;
+    int page_tokens;        /* paged caches: rows per page; 0 for a dense cache */
+    int num_pages;          /* paged caches: pages in each of the K and V pools */
+    int max_pages_per_seq;  /* paged caches: page-table entries per sequence */
 } dkv_cache_info_t;
 
 /* Allocate a K cache and a V cache of [batch][n_kv_heads][max_tokens][head_dim]
@@ -81,6 +84,32 @@ typedef struct {
  * memory), ALLOC. */
 dkv_status dkv_cache_alloc(dkv_cache** out, int batch, int n_kv_heads, int head_dim,
                            int max_tokens, dkv_dtype dtype);
+
+/* A paged cache: K and V pools of [num_pages][n_kv_heads][page_tokens][head_dim]
+ * elements each in pinned, mapped host memory, addressed through a per-
+ * sequence page table (the KV cache pages that the GPU kernels dereference in
+ * place, "DirectKV Guide: Zero-Copy KV Offloading on GH200 & GB200", The
+ * DirectKV Architecture (Zero-Copy Page Management) and End-to-End
+ * Implementation (the page manager, 16-token pages)).  Logical row t of
+ * sequence b lives in pool page table[b][t / page_tokens], row t % page_tokens.
+ * Every decode / prefill call works on paged caches exactly as on dense ones;
+ * a sequence holds at most max_pages_per_seq * page_tokens rows (its
+ * max_tokens).  The page table starts empty (every entry -1).
+ * Errors: as dkv_cache_alloc, plus INVALID_ARG when page_tokens is not a power
+ * of two in [1, 4096] or num_pages / max_pages_per_seq is not positive. */
+dkv_status dkv_cache_alloc_paged(dkv_cache** out, int batch, int n_kv_heads, int head_dim,
+                                 int page_tokens, int num_pages, int max_pages_per_seq,
+                                 dkv_dtype dtype);
+
+/* Replace a paged cache's page table: table is host memory of
+ * [batch][max_pages_per_seq] int32 pool page indices, -1 for none.  The
+ * library keeps a host copy (each call checks that the rows it reads and
+ * appends, [0, len + T) of every sequence, sit on pages: CAPACITY otherwise)
+ * and a device copy, written after the cache's last stream has finished.
+ * Pages may be shared between sequences for reading; the caller must not
+ * let two sequences append into the same page row.
+ * Errors: INVALID_ARG (dense cache, entry outside [-1, num_pages)), CUDA. */
+dkv_status dkv_cache_set_page_table(dkv_cache* cache, const int32_t* table);
 
 /* Release the pinned caches and the device workspace.  The caller must make
  * sure no enqueued work still uses the cache.  A handle already freed (or
@@ -182,7 +211,8 @@ dkv_status dkv_probe_write(void* dst, size_t bytes, void* stream);
  * per (sequence, query head, split) reads its KV head's rows straight from
  * the host cache with no shared-memory tile and no reuse across the heads of
  * a group.  It attends q (HBM, [B, Hq, D], the dtype) over keys 0..len[b]-1
- * of the cache as it stands (no projection, no append) into out [B, Hq, D]. */
+ * of the cache as it stands (no projection, no append) into out [B, Hq, D].
+ * Dense caches only (UNSUPPORTED for a paged cache). */
 dkv_status dkv_attend_naive(dkv_cache* cache, const void* q, int n_q_heads, void* out,
                             void* stream);
 
@@ -190,7 +220,8 @@ dkv_status dkv_attend_naive(dkv_cache* cache, const void* q, int n_q_heads, void
  * DirectKV", Motivation): cudaMemcpyAsync the cached rows [0, len[b]) of
  * every (sequence, KV head) into the caller's HBM buffers k_stage, v_stage
  * (each [B][Hkv][max_tokens][D]) and run the same fused decode as dkv_decode
- * reading the prefix from HBM (the append still goes to the host cache). */
+ * reading the prefix from HBM (the append still goes to the host cache).
+ * Dense caches only (UNSUPPORTED for a paged cache). */
 dkv_status dkv_decode_staged(dkv_cache* cache, const void* x, const void* wq, const void* wk,
                              const void* wv, int hidden, int n_q_heads, void* out,
                              void* k_stage, void* v_stage, void* stream);

@@ -92,14 +92,30 @@ def assert_close_beyond_rounding(got, ref, dtype, what=""):
 class Case:
     """A workload materialised on the GPU and in the host cache."""
 
-    def __init__(self, w: wl.Workload, lens=None, s_max=None, tuning=None):
+    def __init__(self, w: wl.Workload, lens=None, s_max=None, tuning=None, page_tokens=0,
+                 spare_pages=3, table_seed=0):
+        """page_tokens > 0 builds a paged cache: the logical rows of every
+        sequence go to pool pages drawn by a seeded permutation (spare pages
+        stay in no table and hold the 0x5A5A canary)."""
         import zero_copy_offloaded_gb300 as dkv
         self.w = w
         self.dense = wl.make_dense(w)
         self.s_max = s_max or w.S_max
         self.lens = np.broadcast_to(np.asarray(w.P if lens is None else lens, np.int64),
                                     (w.B,)).copy()
-        self.cache = dkv.KVCache(w.B, w.Hkv, w.D, self.s_max, w.dtype)
+        self.page_tokens = page_tokens
+        if page_tokens:
+            npg = -(-self.s_max // page_tokens)
+            self.s_max = npg * page_tokens
+            perm = np.random.default_rng(table_seed).permutation(w.B * npg + spare_pages)
+            self.table = perm[:w.B * npg].reshape(w.B, npg).astype(np.int32)
+            self.spare = perm[w.B * npg:]
+            self.cache = dkv.PagedKVCache(w.B, w.Hkv, w.D, page_tokens, len(perm), npg, w.dtype)
+            self.cache.k_host[...] = 0x5A5A
+            self.cache.v_host[...] = 0x5A5A
+            self.cache.set_page_table(self.table)
+        else:
+            self.cache = dkv.KVCache(w.B, w.Hkv, w.D, self.s_max, w.dtype)
         # prefix rows: the workload's generator, truncated per sequence
         kc = np.zeros((w.B, w.Hkv, self.s_max, w.D), np.uint16)
         vc = np.zeros_like(kc)
@@ -115,8 +131,12 @@ class Case:
                                        >= self.lens[:, None, None, None], kc.shape)] = 0x7E57
         vc[np.broadcast_to(np.arange(self.s_max)[None, None, :, None]
                            >= self.lens[:, None, None, None], vc.shape)] = 0x7E57
-        self.cache.k_host[...] = kc
-        self.cache.v_host[...] = vc
+        if page_tokens:
+            self._scatter(self.cache.k_host, kc)
+            self._scatter(self.cache.v_host, vc)
+        else:
+            self.cache.k_host[...] = kc
+            self.cache.v_host[...] = vc
         self.k0, self.v0 = kc, vc
         self.cache.set_lengths(self.lens.astype(np.int32))
         if tuning:
@@ -125,6 +145,33 @@ class Case:
         self.wq = to_dev(self.dense["wq"], w.dtype)
         self.wk = to_dev(self.dense["wk"], w.dtype)
         self.wv = to_dev(self.dense["wv"], w.dtype)
+
+    def _scatter(self, pool, logical):
+        pt = self.page_tokens
+        for b in range(self.w.B):
+            for i, pg in enumerate(self.table[b]):
+                pool[pg] = logical[b, :, i * pt:(i + 1) * pt]
+
+    def _gather(self, pool):
+        pt = self.page_tokens
+        out = np.empty((self.w.B, self.w.Hkv, self.s_max, self.w.D), np.uint16)
+        for b in range(self.w.B):
+            for i, pg in enumerate(self.table[b]):
+                out[b, :, i * pt:(i + 1) * pt] = pool[pg]
+        return out
+
+    def k_logical(self):
+        """The K cache as [B, Hkv, s_max, D] rows (gathered through the page table)."""
+        return self._gather(self.cache.k_host) if self.page_tokens else self.cache.k_host
+
+    def v_logical(self):
+        return self._gather(self.cache.v_host) if self.page_tokens else self.cache.v_host
+
+    def spare_pages_untouched(self):
+        if not self.page_tokens:
+            return True
+        return bool(np.all(self.cache.k_host[self.spare] == 0x5A5A) and
+                    np.all(self.cache.v_host[self.spare] == 0x5A5A))
 
     def out_tensor(self, T):
         import torch

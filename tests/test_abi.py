@@ -72,6 +72,13 @@ def test_invalid_arguments_fail_before_gpu_work(L):
     assert L.dkv_probe_read(None, 16, None, None) == 1
     assert L.dkv_probe_write(None, 0, None) == 1
     assert "invalid" in dkv.dkv_last_error()
+    # paged caches: page size a power of two, positive pool and table sizes
+    assert L.dkv_cache_alloc_paged(ctypes.byref(h), 1, 1, 128, 12, 4, 4, 0) == 1
+    assert L.dkv_cache_alloc_paged(ctypes.byref(h), 1, 1, 128, 16, 0, 4, 0) == 1
+    assert L.dkv_cache_alloc_paged(ctypes.byref(h), 1, 1, 128, 16, 4, 0, 0) == 1
+    assert L.dkv_cache_alloc_paged(ctypes.byref(h), 1, 1, 96, 16, 4, 4, 0) == 2
+    assert h.value is None
+    assert L.dkv_cache_set_page_table(None, None) == 1
 
 
 def test_binding_raises_typed_errors(L):

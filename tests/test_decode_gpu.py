@@ -19,7 +19,7 @@ def check_decode(case: Case, out, ref, label=""):
     w = case.w
     got = out_f64(out, w.dtype).reshape(w.B, w.Hq, w.D)
     mx, mr = assert_close(got, ref["out"].reshape(w.B, w.Hq, w.D), label)
-    kh, vh = case.cache.k_host, case.cache.v_host
+    kh, vh = case.k_logical(), case.v_logical()
     for b in range(w.B):
         p = int(case.lens[b])
         assert np.array_equal(kh[b, :, p], ref["k_new"][b, 0]), f"{label} k append b={b}"

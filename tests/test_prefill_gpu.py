@@ -30,7 +30,7 @@ def check_prefill(case: Case, out, ref, label="", rows=None, beyond_rounding=Fal
         g = np.stack([got[b, t] for (b, t) in rows])
         r = np.stack([ref["out"][(b, t)] for (b, t) in rows])
         res = assert_close(g, r, label)
-    kh, vh = case.cache.k_host, case.cache.v_host
+    kh, vh = case.k_logical(), case.v_logical()
     x = case.dense["x"]
     for b in range(w.B):
         p = int(case.lens[b])

@@ -23,7 +23,8 @@ __all__ = [
     "dkv_cache_set_tuning", "dkv_decode", "dkv_prefill", "dkv_sync_status", "dkv_status_str",
     "dkv_last_error", "dkv_probe_read", "dkv_probe_write", "dkv_attend_naive",
     "dkv_decode_staged", "dkv_last_launch_count", "dkv_cache_kernel_timing",
-    "dkv_cache_last_kernel_ms",
+    "dkv_cache_last_kernel_ms", "dkv_cache_alloc_paged", "dkv_cache_set_page_table",
+    "PagedKVCache",
 ]
 
 BF16 = 0
@@ -53,7 +54,8 @@ class _CacheInfo(ctypes.Structure):
                 ("device_staging_bytes", ctypes.c_size_t),
                 ("batch", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("max_tokens", ctypes.c_int),
-                ("dtype", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("page_tokens", ctypes.c_int),
+                ("num_pages", ctypes.c_int), ("max_pages_per_seq", ctypes.c_int)]
 
 
 _lib = None
@@ -75,6 +77,8 @@ def lib(build_if_missing: bool = False):
     P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     sig = {
         "dkv_cache_alloc": [ctypes.POINTER(P), I, I, I, I, I],
+        "dkv_cache_alloc_paged": [ctypes.POINTER(P), I, I, I, I, I, I, I],
+        "dkv_cache_set_page_table": [P, P],
         "dkv_free": [P],
         "dkv_cache_host_ptrs": [P, ctypes.POINTER(P), ctypes.POINTER(P)],
         "dkv_cache_device_ptrs": [P, ctypes.POINTER(P), ctypes.POINTER(P)],
@@ -152,6 +156,21 @@ def dkv_cache_alloc(batch, n_kv_heads, head_dim, max_tokens, dtype="bf16") -> in
     _check(lib().dkv_cache_alloc(ctypes.byref(h), batch, n_kv_heads, head_dim, max_tokens,
                                  _DTYPE[dtype]), "dkv_cache_alloc")
     return h.value
+
+
+def dkv_cache_alloc_paged(batch, n_kv_heads, head_dim, page_tokens, num_pages,
+                          max_pages_per_seq, dtype="bf16") -> int:
+    h = ctypes.c_void_p()
+    _check(lib().dkv_cache_alloc_paged(ctypes.byref(h), batch, n_kv_heads, head_dim, page_tokens,
+                                       num_pages, max_pages_per_seq, _DTYPE[dtype]),
+           "dkv_cache_alloc_paged")
+    return h.value
+
+
+def dkv_cache_set_page_table(h, table):
+    """table: int32 [batch, max_pages_per_seq] of pool page indices (-1: none)."""
+    t = np.ascontiguousarray(table, dtype=np.int32)
+    _check(lib().dkv_cache_set_page_table(h, t.ctypes.data), "dkv_cache_set_page_table")
 
 
 def dkv_free(h):
@@ -297,3 +316,27 @@ class KVCache:
             self.free()
         except Exception:
             pass
+
+
+class PagedKVCache(KVCache):
+    """A paged cache: numpy views of the K and V page pools
+    ([num_pages, Hkv, page_tokens, D] uint16 each) and the page table."""
+
+    def __init__(self, batch, n_kv_heads, head_dim, page_tokens, num_pages, max_pages_per_seq,
+                 dtype="bf16"):
+        self.B, self.Hkv, self.D = batch, n_kv_heads, head_dim
+        self.page_tokens, self.num_pages, self.max_pages = page_tokens, num_pages, max_pages_per_seq
+        self.S_max = page_tokens * max_pages_per_seq
+        self.dtype = dtype
+        self.h = dkv_cache_alloc_paged(batch, n_kv_heads, head_dim, page_tokens, num_pages,
+                                       max_pages_per_seq, dtype)
+        kp, vp = dkv_cache_host_ptrs(self.h)
+        shape = (num_pages, n_kv_heads, page_tokens, head_dim)
+        n = int(np.prod(shape))
+        self.k_host = np.ctypeslib.as_array((ctypes.c_uint16 * n).from_address(kp)).reshape(shape)
+        self.v_host = np.ctypeslib.as_array((ctypes.c_uint16 * n).from_address(vp)).reshape(shape)
+        self.table = np.full((batch, max_pages_per_seq), -1, np.int32)
+
+    def set_page_table(self, table):
+        dkv_cache_set_page_table(self.h, table)
+        self.table = np.array(table, dtype=np.int32, copy=True)

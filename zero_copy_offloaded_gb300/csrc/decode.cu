@@ -157,7 +157,7 @@ __device__ void project_columns(const DecodeParams& p, int c_begin, int c_end, u
             T* ws = static_cast<T*>(p.kv_ws) + ((size_t)b * 2 + (which - 1)) * p.Hkv * D + local;
             ws[0] = v0; ws[1] = v1;
             T* host = static_cast<T*>(which == 1 ? p.k_host : p.v_host) +
-                      (((size_t)b * p.Hkv + kvh) * p.S_max + p.len[b]) * D + d;
+                      p.lay.row(b, kvh, p.len[b], D) + d;
             host[0] = v0; host[1] = v1;   // the append: one write across the link
           }
         }
@@ -212,9 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
     int it = 0;
     for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
       const UnitRange r = unit_range(p, u);
-      const size_t head_off = ((size_t)r.b * p.Hkv + r.kvh) * p.S_max * D;
-      const T* kg = static_cast<const T*>(p.k_read) + head_off;
-      const T* vg = static_cast<const T*>(p.v_read) + head_off;
+      const T* kg = static_cast<const T*>(p.k_read);
+      const T* vg = static_cast<const T*>(p.v_read);
       const int cached = p.len[r.b];
       for (int t = r.t_lo; t < r.t_hi; ++t, ++it) {
         const int stage = it % stages;
@@ -232,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
         for (int i = ptid; i < nrows * CPR; i += kProducers) {
           const int row = i / CPR, c = i % CPR;
           const int dst = row * (D * 2) + swz_chunk(row, c) * 16;
-          const size_t src = (size_t)(key0 + row) * D + c * 8;
+          const size_t src = p.lay.row(r.b, r.kvh, key0 + row, D) + c * 8;
           cp_async16(kt + dst, kg + src, 16);
           cp_async16(vt + dst, vg + src, 16);
         }

@@ -149,6 +149,8 @@ extern "C" dkv_status dkv_decode_noalloc(const void* x, const void* wq, const vo
   p.out = out;
   p.B = batch; p.H = hidden; p.Hq = n_q_heads; p.Hkv = n_kv_heads; p.D = D;
   p.S_max = max_tokens;
+  p.lay.Hkv = n_kv_heads;  // dense [B][Hkv][max_tokens][D] caches
+  p.lay.S_max = max_tokens;
   p.splits = splits; p.tile_n = N; p.stages = stages;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   for (int b = 0; b < kMaxBatch; ++b) p.len[b] = b < batch ? lengths[b] : 0;

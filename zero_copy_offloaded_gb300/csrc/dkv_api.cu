@@ -80,6 +80,10 @@ struct dkv_cache {
   KernelTimer timer;      // events around the main fused kernel (measurement)
   bool timer_used;
   int debug_withhold;     // test hook for the bounded-wait path
+  // paged caches (page_tokens == 0: dense [B][Hkv][max_tokens][D])
+  int page_tokens, page_shift, num_pages, max_pages;
+  std::vector<int32_t> pages;  // host copy of the page table [B][max_pages], -1 = none
+  int* pages_dev;              // device copy read by the kernels
   std::mutex mu;
 };
 
@@ -175,7 +179,32 @@ dkv_status check_call(dkv_cache* c, const void* x, const void* wq, const void* w
     if ((long)c->len[b] + T > c->max_tokens)
       return fail(DKV_ERR_CAPACITY, "sequence %d: length %d + %d new > max_tokens %d", b,
                   c->len[b], T, c->max_tokens);
+  if (c->page_tokens) {
+    // every row the call reads or writes, [0, len + T), must sit on a page
+    for (int b = 0; b < c->B; ++b) {
+      const int need = (c->len[b] + T + c->page_tokens - 1) >> c->page_shift;
+      for (int i = 0; i < need; ++i)
+        if (c->pages[(size_t)b * c->max_pages + i] < 0)
+          return fail(DKV_ERR_CAPACITY, "sequence %d: logical page %d (of %d needed) has no page",
+                      b, i, need);
+    }
+  }
   return DKV_OK;
+}
+
+size_t pool_rows(const dkv_cache* c) {
+  return c->page_tokens ? (size_t)c->num_pages * c->Hkv * c->page_tokens
+                        : (size_t)c->B * c->Hkv * c->max_tokens;
+}
+
+CacheLayout layout_of(const dkv_cache* c) {
+  CacheLayout l;
+  l.pages = c->page_tokens ? c->pages_dev : nullptr;
+  l.page_shift = c->page_shift;
+  l.max_pages = c->max_pages;
+  l.Hkv = c->Hkv;
+  l.S_max = c->max_tokens;
+  return l;
 }
 
 void fill_lens(int* dst, const std::vector<int32_t>& len) {
@@ -219,6 +248,7 @@ dkv_status decode_impl(dkv_cache* c, const void* x, const void* wq, const void* 
   p.splits = ch.splits; p.tile_n = ch.tile_n; p.stages = ch.stages;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   p.debug_withhold = c->debug_withhold;
+  p.lay = layout_of(c);
   fill_lens(p.len, c->len);
   g_last_launches = 0;
   cudaError_t e = launch_decode(p, c->dtype, ch.grid, ch.smem, s, &g_last_launches, c->timer);
@@ -254,8 +284,11 @@ const char* dkv_last_error(void) { return g_last_error.c_str(); }
 
 int dkv_last_launch_count(void) { return g_last_launches; }
 
-dkv_status dkv_cache_alloc(dkv_cache** out, int batch, int n_kv_heads, int head_dim,
-                           int max_tokens, dkv_dtype dtype) {
+// Shared by the dense and the paged allocation: `rows` cache rows of D
+// elements each for K and for V in pinned, mapped host memory.
+static dkv_status alloc_common(dkv_cache** out, int batch, int n_kv_heads, int head_dim,
+                               int max_tokens, dkv_dtype dtype, size_t rows, int page_tokens,
+                               int num_pages, int max_pages) {
   if (!out) return fail(DKV_ERR_INVALID_ARG, "null output handle");
   *out = nullptr;
   if (batch <= 0 || batch > kMaxBatch)
@@ -279,8 +312,7 @@ dkv_status dkv_cache_alloc(dkv_cache** out, int batch, int n_kv_heads, int head_
   cudaDeviceGetAttribute(&can_map, cudaDevAttrCanMapHostMemory, dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (!can_map) return fail(DKV_ERR_NO_MAPPED_MEMORY, "device %d cannot map host memory", dev);
-  const size_t elems = (size_t)batch * n_kv_heads * max_tokens * head_dim;
-  const size_t bytes = elems * 2;
+  const size_t bytes = rows * head_dim * 2;
   void* kh = nullptr;
   void* vh = nullptr;
   e = cudaHostAlloc(&kh, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
@@ -312,6 +344,18 @@ dkv_status dkv_cache_alloc(dkv_cache** out, int batch, int n_kv_heads, int head_
     cudaFreeHost(vh);
     return fail(DKV_ERR_ALLOC, "status cudaMalloc: %s", cudaGetErrorString(e));
   }
+  int* pages_dev = nullptr;
+  const size_t table = (size_t)batch * max_pages;
+  if (page_tokens) {
+    if ((e = cudaMalloc(&pages_dev, table * sizeof(int32_t))) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(st);
+      cudaFreeHost(kh);
+      cudaFreeHost(vh);
+      return fail(DKV_ERR_ALLOC, "page table cudaMalloc: %s", cudaGetErrorString(e));
+    }
+    cudaMemset(pages_dev, 0xff, table * sizeof(int32_t));  // -1: no page
+  }
   cudaMemset(st, 0, sizeof(DeviceStatus));
   cudaDeviceSynchronize();
   dkv_cache* c = new dkv_cache;
@@ -327,9 +371,71 @@ dkv_status dkv_cache_alloc(dkv_cache** out, int batch, int n_kv_heads, int head_
   c->tune_splits = c->tune_tile = c->tune_stages = 0;
   c->timer_used = false;
   c->debug_withhold = 0;
+  c->page_tokens = page_tokens;
+  c->page_shift = 0;
+  while (page_tokens && (1 << c->page_shift) < page_tokens) ++c->page_shift;
+  c->num_pages = num_pages;
+  c->max_pages = max_pages;
+  c->pages.assign(table, -1);
+  c->pages_dev = pages_dev;
   *out = c;
   return DKV_OK;
 }
+
+dkv_status dkv_cache_alloc(dkv_cache** out, int batch, int n_kv_heads, int head_dim,
+                           int max_tokens, dkv_dtype dtype) {
+  if (!out) return fail(DKV_ERR_INVALID_ARG, "null output handle");
+  *out = nullptr;
+  if (batch <= 0 || batch > kMaxBatch)
+    return fail(DKV_ERR_INVALID_ARG, "batch=%d must be in [1, %d]", batch, kMaxBatch);
+  if (n_kv_heads <= 0 || max_tokens <= 0)
+    return fail(DKV_ERR_INVALID_ARG, "n_kv_heads=%d and max_tokens=%d must be positive",
+                n_kv_heads, max_tokens);
+  return alloc_common(out, batch, n_kv_heads, head_dim, max_tokens, dtype,
+                      (size_t)batch * n_kv_heads * max_tokens, 0, 0, 0);
+}
+
+dkv_status dkv_cache_alloc_paged(dkv_cache** out, int batch, int n_kv_heads, int head_dim,
+                                 int page_tokens, int num_pages, int max_pages_per_seq,
+                                 dkv_dtype dtype) {
+  if (!out) return fail(DKV_ERR_INVALID_ARG, "null output handle");
+  *out = nullptr;
+  if (batch <= 0 || batch > kMaxBatch)
+    return fail(DKV_ERR_INVALID_ARG, "batch=%d must be in [1, %d]", batch, kMaxBatch);
+  if (n_kv_heads <= 0 || num_pages <= 0 || max_pages_per_seq <= 0)
+    return fail(DKV_ERR_INVALID_ARG, "n_kv_heads=%d, num_pages=%d and max_pages_per_seq=%d "
+                "must be positive", n_kv_heads, num_pages, max_pages_per_seq);
+  if (page_tokens < 1 || page_tokens > 4096 || (page_tokens & (page_tokens - 1)))
+    return fail(DKV_ERR_INVALID_ARG, "page_tokens=%d must be a power of two in [1, 4096]",
+                page_tokens);
+  if ((long long)max_pages_per_seq * page_tokens > (1LL << 30))
+    return fail(DKV_ERR_INVALID_ARG, "max_pages_per_seq * page_tokens is too large");
+  return alloc_common(out, batch, n_kv_heads, head_dim, max_pages_per_seq * page_tokens, dtype,
+                      (size_t)num_pages * n_kv_heads * page_tokens, page_tokens, num_pages,
+                      max_pages_per_seq);
+}
+
+dkv_status dkv_cache_set_page_table(dkv_cache* c, const int32_t* table) {
+  if (!valid(c) || !table) return fail(DKV_ERR_INVALID_ARG, "invalid argument");
+  if (!c->page_tokens) return fail(DKV_ERR_INVALID_ARG, "the cache is dense, not paged");
+  const size_t n = c->pages.size();
+  for (size_t i = 0; i < n; ++i)
+    if (table[i] < -1 || table[i] >= c->num_pages)
+      return fail(DKV_ERR_INVALID_ARG, "page table entry %zu = %d outside [-1, %d)", i, table[i],
+                  c->num_pages);
+  std::lock_guard<std::mutex> lk(c->mu);
+  dkv_status st = set_device(c);
+  if (st != DKV_OK) return st;
+  // enqueued calls may still read the previous table
+  cudaError_t e = cudaStreamSynchronize(c->last_stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(c->pages_dev, table, n * sizeof(int32_t), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "page table copy");
+  c->pages.assign(table, table + n);
+  return DKV_OK;
+}
+
+
 
 dkv_status dkv_free(dkv_cache* c) {
   if (!valid(c)) return fail(DKV_ERR_INVALID_ARG, "invalid or already freed cache handle");
@@ -341,6 +447,8 @@ dkv_status dkv_free(dkv_cache* c) {
   if (c->timer.stop) cudaEventDestroy(c->timer.stop);
   c->timer = KernelTimer();
   cudaFree(c->status);
+  if (c->pages_dev) cudaFree(c->pages_dev);
+  c->pages_dev = nullptr;
   cudaFreeHost(c->k_host);
   cudaFreeHost(c->v_host);
   // The handle memory is kept (tagged dead) so a second free is detected
@@ -384,11 +492,14 @@ dkv_status dkv_cache_get_lengths(const dkv_cache* c, int32_t* len) {
 
 dkv_status dkv_cache_info(const dkv_cache* c, dkv_cache_info_t* info) {
   if (!valid(c) || !info) return fail(DKV_ERR_INVALID_ARG, "invalid argument");
-  info->host_pinned_bytes = 2 * (size_t)c->B * c->Hkv * c->max_tokens * c->D * 2;
-  info->device_workspace_bytes = c->ws.bytes + sizeof(DeviceStatus);
+  info->host_pinned_bytes = 2 * pool_rows(c) * c->D * 2;
+  info->device_workspace_bytes = c->ws.bytes + sizeof(DeviceStatus) +
+                                 c->pages.size() * sizeof(int32_t);
   info->device_staging_bytes = 0;
   info->batch = c->B; info->n_kv_heads = c->Hkv; info->head_dim = c->D;
   info->max_tokens = c->max_tokens; info->dtype = c->dtype;
+  info->page_tokens = c->page_tokens; info->num_pages = c->num_pages;
+  info->max_pages_per_seq = c->max_pages;
   return DKV_OK;
 }
 
@@ -449,6 +560,7 @@ dkv_status dkv_decode_staged(dkv_cache* c, const void* x, const void* wq, const 
   dkv_status st = check_call(c, x, wq, wk, wv, hidden, n_q_heads, out, 1);
   if (st != DKV_OK) return st;
   if (!k_stage || !v_stage) return fail(DKV_ERR_INVALID_ARG, "null staging buffer");
+  if (c->page_tokens) return fail(DKV_ERR_UNSUPPORTED, "staged decode needs a dense cache");
   std::lock_guard<std::mutex> lk(c->mu);
   if ((st = set_device(c)) != DKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -502,6 +614,7 @@ dkv_status dkv_prefill(dkv_cache* c, const void* x, int T, const void* wq, const
   p.B = B; p.T = T; p.H = hidden; p.Hq = Hq; p.Hkv = c->Hkv; p.D = D; p.S_max = c->max_tokens;
   p.chunk = C; p.nchunks = nchunks;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  p.lay = layout_of(c);
   fill_lens(p.len, c->len);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   g_last_launches = 0;
@@ -594,6 +707,7 @@ dkv_status dkv_probe_write(void* dst, size_t bytes, void* stream) {
 dkv_status dkv_attend_naive(dkv_cache* c, const void* q, int n_q_heads, void* out, void* stream) {
   if (!valid(c) || !q || !out || n_q_heads <= 0 || n_q_heads % c->Hkv)
     return fail(DKV_ERR_INVALID_ARG, "invalid argument");
+  if (c->page_tokens) return fail(DKV_ERR_UNSUPPORTED, "naive attention needs a dense cache");
   std::lock_guard<std::mutex> lk(c->mu);
   dkv_status st = set_device(c);
   if (st != DKV_OK) return st;

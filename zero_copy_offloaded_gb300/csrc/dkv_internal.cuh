@@ -153,6 +153,25 @@ struct LenArray {
   int v[kMaxBatch];
 };
 
+// Where cache row `tok` of (sequence b, KV head kvh) lives, as an element
+// offset from the K (or V) base.  Dense caches are [B][Hkv][S_max][D]; paged
+// caches are a pool [page][Hkv][page_tokens][D] with a per-sequence page table
+// (logical page i of sequence b is pool page pages[b * max_pages + i]), so a
+// page holds page_tokens contiguous rows of one KV head.
+struct CacheLayout {
+  const int* pages;  // device [B][max_pages]; null for a dense cache
+  int page_shift;    // log2(page_tokens)
+  int max_pages;
+  int Hkv;
+  int S_max;         // dense: rows per (b, KV head)
+  __device__ __forceinline__ size_t row(int b, int kvh, int tok, int D) const {
+    if (!pages) return (((size_t)b * Hkv + kvh) * S_max + tok) * (size_t)D;
+    const int pg = __ldg(pages + (size_t)b * max_pages + (tok >> page_shift));
+    return ((((size_t)pg * Hkv + kvh) << page_shift) + (tok & ((1 << page_shift) - 1))) *
+           (size_t)D;
+  }
+};
+
 struct DecodeParams {
   // inputs (device)
   const void* x;    // [B, H]
@@ -178,6 +197,7 @@ struct DecodeParams {
   int stages;
   float scale_log2;  // log2(e) / sqrt(D)
   int debug_withhold;  // test hook: producers never signal their first tile
+  CacheLayout lay;     // rows of k_read / v_read / k_host / v_host
   int len[kMaxBatch];
 };
 
@@ -199,6 +219,7 @@ struct PrefillParams {
   int chunk;         // keys per stationary chunk
   int nchunks;       // chunks per sequence (max over the batch)
   float scale_log2;
+  CacheLayout lay;   // rows of k_read / v_read / k_host / v_host
   int len[kMaxBatch];
 };
 
