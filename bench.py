@@ -156,6 +156,11 @@ def sweep(args, dkv, torch, dev, stream, flush, pk):
             dkv.dkv_decode_staged(cache.h, x, wq, wk, wv, w.H, w.Hq, out, ks, vs, stream)
         staged_ms = min(_time_once(torch, stream, flush, staged) for _ in range(3))
         del ks, vs
+
+        def unfused():
+            cache.set_lengths(lens)
+            dkv.dkv_decode_unfused(cache.h, x, wq, wk, wv, w.H, w.Hq, out, stream)
+        unfused_ms = min(_time_once(torch, stream, flush, unfused) for _ in range(3))
         cache.free()
         step_ms = statistics.median(ms)
         hb = w.host_read_bytes()
@@ -164,7 +169,8 @@ def sweep(args, dkv, torch, dev, stream, flush, pk):
             "Hkv": w.Hkv, "dtype": w.dtype, "step_ms": step_ms, "tok_s": w.B / (step_ms * 1e-3),
             "fused_kernel_ms": kern, "host_link_gbs": hb / (kern * 1e-3) / 1e9,
             "frac_of_link": hb / (kern * 1e-3) / 1e9 / link_rd,
-            "naive_zero_copy_ms": naive, "copy_to_hbm_then_attend_ms": staged_ms}), flush=True)
+            "naive_zero_copy_ms": naive, "copy_to_hbm_then_attend_ms": staged_ms,
+            "separate_kernels_ms": unfused_ms}), flush=True)
     for name in ("llama8b_decode", "longctx_b1_s128k"):
         res = bench_paged_decode(wl.WORKLOADS[name], 16, dkv, torch, dev, stream, flush, link_rd,
                                  args.steps)
@@ -480,10 +486,16 @@ def main():
             dkv.dkv_decode_staged(cache.h, x, wq, wk, wv, w.H, w.Hq, out, ks, vs, stream)
         staged_ms = time_kernel(staged, reps=3)
         del ks, vs
+
+        def unfused():
+            cache.set_lengths(lens)
+            dkv.dkv_decode_unfused(cache.h, x, wq, wk, wv, w.H, w.Hq, out, stream)
+        unfused_ms = time_kernel(unfused, reps=3)
         extras["baselines"] = {
             "fused_zero_copy_step_ms": statistics.mean(step_ms),
             "naive_zero_copy_attention_ms": naive_ms,
             "copy_to_hbm_then_attend_ms": staged_ms,
+            "separate_kernels_ms": unfused_ms,
             "hbm_staging_bytes": 2 * cache_bytes,
         }
         extras["prefill"] = bench_prefill(args, dkv, torch, dev, stream, flush, pk, link_rd,

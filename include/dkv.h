@@ -216,6 +216,17 @@ dkv_status dkv_probe_write(void* dst, size_t bytes, void* stream);
 dkv_status dkv_attend_naive(dkv_cache* cache, const void* q, int n_q_heads, void* out,
                             void* stream);
 
+/* Separate-kernel baseline (the unfused design the pages compare against,
+ * "Paper Notes: DirectKV", Experiments & Results, Fused kernel (Fig. 13), and
+ * Key Ideas (2)): the same
+ * decode as dkv_decode split into two launches, a projection that writes q to
+ * HBM and appends the fresh K/V rows to the host cache, then an attention
+ * launch that reads every row, the appended one included, back across the
+ * link.  Same arguments, results and errors as dkv_decode. */
+dkv_status dkv_decode_unfused(dkv_cache* cache, const void* x, const void* wq, const void* wk,
+                              const void* wv, int hidden, int n_q_heads, void* out,
+                              void* stream);
+
 /* Copy-to-HBM-then-attend baseline (swap-style staging, "Paper Notes:
  * DirectKV", Motivation): cudaMemcpyAsync the cached rows [0, len[b]) of
  * every (sequence, KV head) into the caller's HBM buffers k_stage, v_stage

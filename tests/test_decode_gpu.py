@@ -98,6 +98,29 @@ def test_decode_two_steps():
         case.free()
 
 
+@pytest.mark.parametrize("page_tokens", [0, 16])
+@pytest.mark.parametrize("dtype,D,Hq,Hkv", [("bf16", 128, 32, 8), ("fp16", 64, 8, 8)])
+def test_decode_unfused_baseline(dtype, D, Hq, Hkv, page_tokens):
+    """The separate-kernel baseline (a projection launch that appends, then an
+    attention launch that reads every row, the new one included, from the
+    host cache) meets the same bars: bit-exact appends, outputs within the
+    tolerances."""
+    import zero_copy_offloaded_gb300 as dkv
+    w = wl.Workload("t", "decode", B=3, H=256, Hq=Hq, Hkv=Hkv, D=D, P=333, dtype=dtype,
+                    kv_dist="uniform2" if dtype == "fp16" else "normal", seed=17)
+    case = Case(w, lens=[333, 0, 64], s_max=340, page_tokens=page_tokens)
+    try:
+        out = case.out_tensor(1)
+        dkv.dkv_decode_unfused(case.cache.h, case.x.reshape(w.B, 1, w.H), case.wq, case.wk,
+                               case.wv, w.H, w.Hq, out, None)
+        case.cache.sync()
+        check_decode(case, out, case.oracle(), f"unfused {dtype} pages={page_tokens}")
+        assert list(case.cache.lengths()) == [334, 1, 65]
+        assert dkv.dkv_last_launch_count() == 3
+    finally:
+        case.free()
+
+
 def test_decode_tiny_workload_full_size():
     case = Case(wl.WORKLOADS["tiny_decode"])
     try:

@@ -22,7 +22,7 @@ __all__ = [
     "dkv_cache_set_lengths", "dkv_cache_get_lengths", "dkv_cache_info", "dkv_cache_reserve",
     "dkv_cache_set_tuning", "dkv_decode", "dkv_prefill", "dkv_sync_status", "dkv_status_str",
     "dkv_last_error", "dkv_probe_read", "dkv_probe_write", "dkv_attend_naive",
-    "dkv_decode_staged", "dkv_last_launch_count", "dkv_cache_kernel_timing",
+    "dkv_decode_staged", "dkv_decode_unfused", "dkv_last_launch_count", "dkv_cache_kernel_timing",
     "dkv_cache_last_kernel_ms", "dkv_cache_alloc_paged", "dkv_cache_set_page_table",
     "PagedKVCache",
 ]
@@ -94,6 +94,7 @@ def lib(build_if_missing: bool = False):
         "dkv_probe_write": [P, Z, P],
         "dkv_attend_naive": [P, P, I, P, P],
         "dkv_decode_staged": [P, P, P, P, P, I, I, P, P, P, P],
+        "dkv_decode_unfused": [P, P, P, P, P, I, I, P, P],
         "dkv_cache_kernel_timing": [P, I],
         "dkv_cache_last_kernel_ms": [P, ctypes.POINTER(ctypes.c_float)],
         "dkv_decode_noalloc": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P],
@@ -259,6 +260,11 @@ def dkv_probe_write(dst, nbytes, stream=None):
 def dkv_attend_naive(h, q, n_q_heads, out, stream=None):
     _check(lib().dkv_attend_naive(h, _ptr(q), n_q_heads, _ptr(out), _stream(stream)),
            "dkv_attend_naive")
+
+
+def dkv_decode_unfused(h, x, wq, wk, wv, hidden, n_q_heads, out, stream=None):
+    _check(lib().dkv_decode_unfused(h, _ptr(x), _ptr(wq), _ptr(wk), _ptr(wv), hidden, n_q_heads,
+                                    _ptr(out), _stream(stream)), "dkv_decode_unfused")
 
 
 def dkv_decode_staged(h, x, wq, wk, wv, hidden, n_q_heads, out, k_stage, v_stage, stream=None):

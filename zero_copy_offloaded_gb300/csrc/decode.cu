@@ -22,6 +22,9 @@
 //            compute the G heads' scores, the online softmax and P.V in fp32
 //            and write one normalised partial (o, lse) per unit.
 // The combine kernel merges the splits with a log-sum-exp weighting.
+// The same kernel also runs the two halves of the separate-kernel baseline
+// (DecodeMode): phase A alone, then phase B over rows that all come from the
+// host cache, the freshly appended one included.
 #include "dkv_internal.cuh"
 
 namespace dkv {
@@ -208,13 +211,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
 
   if (tid >= kConsumers) {
     // ------------------------------------------------------------ producer
+    if (p.mode == kDecodeProjectOnly) return;
     const int ptid = tid - kConsumers;
     int it = 0;
     for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
       const UnitRange r = unit_range(p, u);
       const T* kg = static_cast<const T*>(p.k_read);
       const T* vg = static_cast<const T*>(p.v_read);
-      const int cached = p.len[r.b];
+      // rows read from the host: the cached ones (the fused path takes the new
+      // row from HBM), or every row when the projection ran as its own launch
+      const int cached = p.len[r.b] + (p.mode == kDecodeAttendOnly ? 1 : 0);
       for (int t = r.t_lo; t < r.t_hi; ++t, ++it) {
         const int stage = it % stages;
         const uint32_t par = ((it / stages) & 1) ^ 1;
@@ -227,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
         uint8_t* kt = smem + L.ring + stage * 2 * tile_bytes;
         uint8_t* vt = kt + tile_bytes;
         const int key0 = t * N;
-        const int nrows = max(0, min(N, cached - key0));  // host rows only; the new row comes from HBM
+        const int nrows = max(0, min(N, cached - key0));
         for (int i = ptid; i < nrows * CPR; i += kProducers) {
           const int row = i / CPR, c = i % CPR;
           const int dst = row * (D * 2) + swz_chunk(row, c) * 16;
@@ -249,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
   const int warp = ctid / 32, lane = ctid % 32;
 
   // Phase A: projection slice of this CTA.
-  {
+  if (p.mode != kDecodeAttendOnly) {
     const int ncol = (p.Hq + 2 * p.Hkv) * D;
     const int nblk = ncol / 8;
     const int per = nblk / gridDim.x, rem = nblk % gridDim.x;
@@ -257,22 +263,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
     const int b1 = b0 + per + ((int)blockIdx.x < rem ? 1 : 0);
     if (b1 > b0) project_columns<T, D>(p, b0 * 8, b1 * 8, smem, L, ctid);
   }
-  // Grid barrier: every CTA's q and fresh k/v are in the workspace.
-  named_bar_sync(kBarConsumers, kConsumers);
-  if (ctid == 0) {
-    __threadfence();
-    atomicAdd(&p.status->grid_arrive, 1u);
-    const uint64_t deadline = global_timer_ns() + kWaitBudgetNs;
-    while (ld_acquire_gpu(&p.status->grid_arrive) < gridDim.x) {
-      if (global_timer_ns() > deadline) {
-        record_timeout(p.status, kSiteGridBarrier);
-        *abort_flag = 1;
-        break;
+  if (p.mode == kDecodeProjectOnly) return;  // the producers returned at once
+  if (p.mode == kDecodeFused) {
+    // Grid barrier: every CTA's q and fresh k/v are in the workspace.  (The
+    // attention-only launch follows the projection launch on the stream.)
+    named_bar_sync(kBarConsumers, kConsumers);
+    if (ctid == 0) {
+      __threadfence();
+      atomicAdd(&p.status->grid_arrive, 1u);
+      const uint64_t deadline = global_timer_ns() + kWaitBudgetNs;
+      while (ld_acquire_gpu(&p.status->grid_arrive) < gridDim.x) {
+        if (global_timer_ns() > deadline) {
+          record_timeout(p.status, kSiteGridBarrier);
+          *abort_flag = 1;
+          break;
+        }
       }
     }
+    named_bar_sync(kBarConsumers, kConsumers);
+    if (*abort_flag) return;  // producers see the flag in their bounded waits
   }
-  named_bar_sync(kBarConsumers, kConsumers);
-  if (*abort_flag) return;  // producers see the flag in their bounded waits
 
   float* q_s = reinterpret_cast<float*>(smem + L.q);     // [G][D+4]
   float* s_s = reinterpret_cast<float*>(smem + L.s);     // [2][G][N]
@@ -322,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
       }
       // the new token's row (if in this tile) comes from the HBM workspace
       const int rnew = p.len[r.b] - key0;
-      if (rnew >= 0 && rnew < N && ctid < 2 * CPR) {
+      if (p.mode == kDecodeFused && rnew >= 0 && rnew < N && ctid < 2 * CPR) {
         const int which = ctid / CPR, c = ctid % CPR;
         const T* src = static_cast<const T*>(p.kv_ws) +
                        ((size_t)r.b * 2 + which) * p.Hkv * D + r.kvh * D + c * 8;
@@ -475,6 +485,7 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, int smem, cudaStrea
                                   (size_t)smem, s);
   if (e != cudaSuccess) return e;
   timer.after(s);
+  if (p.mode == kDecodeProjectOnly) return cudaSuccess;
   decode_combine_kernel<T><<<p.B * p.Hq, D, 0, s>>>(p.part_o, p.part_lse,
                                                     static_cast<T*>(p.out), p.splits, D,
                                                     p.status);
@@ -536,7 +547,7 @@ cudaError_t launch_decode(const DecodeParams& p, int dtype, int grid, int smem_b
                           cudaStream_t s, int* launches, const KernelTimer& timer) {
   LaunchDecodeF f{&p, grid, smem_bytes, s, &timer};
   cudaError_t e = dispatch(dtype, p.D, p.Hq / p.Hkv, f);
-  if (e == cudaSuccess && launches) *launches += 2;
+  if (e == cudaSuccess && launches) *launches += p.mode == kDecodeProjectOnly ? 1 : 2;
   return e;
 }
 

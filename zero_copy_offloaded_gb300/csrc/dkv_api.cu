@@ -216,10 +216,11 @@ dkv_status set_device(dkv_cache* c) {
   return e == cudaSuccess ? DKV_OK : cuda_fail(e, "cudaSetDevice");
 }
 
-// Shared by dkv_decode and dkv_decode_staged.
+// Shared by dkv_decode, dkv_decode_staged and dkv_decode_unfused.
 dkv_status decode_impl(dkv_cache* c, const void* x, const void* wq, const void* wk,
                        const void* wv, int hidden, int n_q_heads, void* out,
-                       const void* k_read, const void* v_read, cudaStream_t s) {
+                       const void* k_read, const void* v_read, cudaStream_t s,
+                       bool unfused = false) {
   const int G = n_q_heads / c->Hkv;
   if (!decode_supported(c->dtype, c->D, G))
     return fail(DKV_ERR_UNSUPPORTED, "no decode kernel for dtype=%d D=%d G=%d", c->dtype, c->D, G);
@@ -251,7 +252,16 @@ dkv_status decode_impl(dkv_cache* c, const void* x, const void* wq, const void* 
   p.lay = layout_of(c);
   fill_lens(p.len, c->len);
   g_last_launches = 0;
-  cudaError_t e = launch_decode(p, c->dtype, ch.grid, ch.smem, s, &g_last_launches, c->timer);
+  cudaError_t e;
+  if (unfused) {  // projection + append, then attention over host rows only
+    p.mode = kDecodeProjectOnly;
+    e = launch_decode(p, c->dtype, ch.grid, ch.smem, s, &g_last_launches, KernelTimer());
+    p.mode = kDecodeAttendOnly;
+    if (e == cudaSuccess)
+      e = launch_decode(p, c->dtype, ch.grid, ch.smem, s, &g_last_launches, c->timer);
+  } else {
+    e = launch_decode(p, c->dtype, ch.grid, ch.smem, s, &g_last_launches, c->timer);
+  }
   c->timer_used = c->timer.start != nullptr;
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -552,6 +562,16 @@ dkv_status dkv_decode(dkv_cache* c, const void* x, const void* wq, const void* w
   if ((st = set_device(c)) != DKV_OK) return st;
   return decode_impl(c, x, wq, wk, wv, hidden, n_q_heads, out, c->k_dev, c->v_dev,
                      static_cast<cudaStream_t>(stream));
+}
+
+dkv_status dkv_decode_unfused(dkv_cache* c, const void* x, const void* wq, const void* wk,
+                              const void* wv, int hidden, int n_q_heads, void* out, void* stream) {
+  dkv_status st = check_call(c, x, wq, wk, wv, hidden, n_q_heads, out, 1);
+  if (st != DKV_OK) return st;
+  std::lock_guard<std::mutex> lk(c->mu);
+  if ((st = set_device(c)) != DKV_OK) return st;
+  return decode_impl(c, x, wq, wk, wv, hidden, n_q_heads, out, c->k_dev, c->v_dev,
+                     static_cast<cudaStream_t>(stream), true);
 }
 
 dkv_status dkv_decode_staged(dkv_cache* c, const void* x, const void* wq, const void* wk,

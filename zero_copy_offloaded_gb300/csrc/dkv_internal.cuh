@@ -172,6 +172,11 @@ struct CacheLayout {
   }
 };
 
+// What one decode launch does: the fused path, or one of the two halves of
+// the separate-kernel baseline (projection + append; then attention over
+// every row read from the host cache, the appended one included).
+enum DecodeMode : int { kDecodeFused = 0, kDecodeProjectOnly = 1, kDecodeAttendOnly = 2 };
+
 struct DecodeParams {
   // inputs (device)
   const void* x;    // [B, H]
@@ -198,6 +203,7 @@ struct DecodeParams {
   float scale_log2;  // log2(e) / sqrt(D)
   int debug_withhold;  // test hook: producers never signal their first tile
   CacheLayout lay;     // rows of k_read / v_read / k_host / v_host
+  int mode;            // DecodeMode
   int len[kMaxBatch];
 };
 
