@@ -618,20 +618,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // out[b,t,h,:] = sum_c w_c 2^k_c o'_c / sum_c w_c, w_c = 2^(lse_c - max lse),
-// over the chunks c = 0 .. (len+t)/C that row sees.  D/8 threads per row, each
-// owning 8 consecutive outputs (16-byte loads of the fp16 partials).
+// over the chunks c = 0 .. (len+t)/C that row sees, in one pass with a running
+// max (what is accumulated is rescaled when a chunk's lse exceeds it).  D/16
+// threads per row, each owning 16 consecutive outputs: two 16-byte loads of
+// the fp16 partials per chunk (32 contiguous bytes per thread).
 template <typename T, int D>
 __global__ void __launch_bounds__(128) prefill_combine_tc_kernel(
     const __half* __restrict__ part_o, const float* __restrict__ part_lse,
     const int* __restrict__ part_k, T* __restrict__ out, LenArray len, int B, int T_, int Hq,
     int Hkv) {
-  constexpr int TPR = D / 8;            // threads per row
+  constexpr int TPR = D / 16;           // threads per row
   constexpr int RPB = 128 / TPR;        // rows per block
   const size_t R = (size_t)B * T_ * Hq;
   const int sub = threadIdx.x % TPR;
   size_t row = (size_t)blockIdx.x * RPB + threadIdx.x / TPR;
   const bool active = row < R;
-  if (!active) row = R - 1;             // keep every lane in the shuffles
+  if (!active) row = R - 1;
   const int h = row % Hq;
   const int bt = row / Hq;
   const int t = bt % T_, b = bt / T_;
@@ -641,20 +643,28 @@ __global__ void __launch_bounds__(128) prefill_combine_tc_kernel(
   const size_t pr = (size_t)kh * T_ * G + (size_t)t * G + h % G;
   const int last = (len.v[b] + t) / kC;
   float M = -INFINITY;
-  for (int c = sub; c <= last; c += TPR) M = fmaxf(M, __ldg(part_lse + c * R + pr));
+  float acc[16];
 #pragma unroll
-  for (int off = TPR / 2; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int e = 0; e < 16; ++e) acc[e] = 0.f;
   float den = 0.f;
-#pragma unroll 4
+#pragma unroll 2
   for (int c = 0; c <= last; ++c) {
-    const float w = exp2f(__ldg(part_lse + c * R + pr) - M);
-    const float wk = ldexpf(w, __ldg(part_k + (size_t)c * B * Hkv + kh));
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(part_o + (c * R + pr) * D) + sub);
-    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+    const float lc = __ldg(part_lse + c * R + pr);
+    if (lc > M) {  // new running max: rescale what is accumulated (0 at the start)
+      const float sc = exp2f(M - lc);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+      for (int e = 0; e < 16; ++e) acc[e] *= sc;
+      den *= sc;
+      M = lc;
+    }
+    const float w = exp2f(lc - M);
+    const float wk = ldexpf(w, __ldg(part_k + (size_t)c * B * Hkv + kh));
+    const uint4* src = reinterpret_cast<const uint4*>(part_o + (c * R + pr) * D) + 2 * sub;
+    const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
+    const uint32_t w8[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w8[e]));
       acc[2 * e] = fmaf(wk, f.x, acc[2 * e]);
       acc[2 * e + 1] = fmaf(wk, f.y, acc[2 * e + 1]);
     }
@@ -662,10 +672,12 @@ __global__ void __launch_bounds__(128) prefill_combine_tc_kernel(
   }
   if (active) {
     const float inv = 1.f / den;
-    uint32_t r[8];
+    uint32_t r[16];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(acc[e]);
-    reinterpret_cast<uint4*>(out + row * D)[sub] = pack8<T>(r, inv);
+    for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(acc[e]);
+    uint4* dst = reinterpret_cast<uint4*>(out + row * D) + 2 * sub;
+    dst[0] = pack8<T>(r, inv);
+    dst[1] = pack8<T>(r + 8, inv);
   }
 }
 
@@ -689,7 +701,7 @@ cudaError_t launch_t(const TcArgs& args, const CUtensorMap& mq, const CUtensorMa
   LenArray len;
   for (int i = 0; i < kMaxBatch; ++i) len.v[i] = args.len[i];
   const size_t R = (size_t)args.B * args.T * args.Hq;
-  constexpr int RPB = 128 / (D / 8);
+  constexpr int RPB = 128 / (D / 16);
   prefill_combine_tc_kernel<T, D><<<(unsigned)((R + RPB - 1) / RPB), 128, 0, s>>>(
       static_cast<const __half*>(args.part_o), args.part_lse, args.part_k, static_cast<T*>(out),
       len, args.B, args.T, args.Hq, args.Hkv);
