@@ -101,6 +101,61 @@ def bench_paged_decode(w, page_tokens, dkv, torch, dev, stream, flush, link_rd, 
             "host_link_gbs": gbs, "frac_of_link": gbs / link_rd}
 
 
+def bench_multilayer(dkv, torch, dev, stream, flush, link_rd, steps, layers=32, B=1, P=4096):
+    """A whole decode step of a `layers`-layer model with Llama-3-8B attention
+    shapes (32/8 heads, D = 128, H = 4096), per-layer caches of B x P tokens
+    in one layered pinned allocation, distinct seeded weights per layer:
+    per-layer launches against one captured graph per step.  The caches grow
+    by one row per step (capacity for every step is allocated)."""
+    H, Hq, Hkv, D = 4096, 32, 8, 128
+    w = wl.Workload("layer", "decode", B=B, H=H, Hq=Hq, Hkv=Hkv, D=D, P=P)
+    total = 2 * (steps + 8) + 2
+    cache = dkv.LayeredKVCache(layers, B, Hkv, D, P + total, "bf16")
+    for l in range(layers):
+        wl_l = w.with_(seed=1000 + l)
+        for b in range(B):
+            for h in range(Hkv):
+                kk, vv = wl.cache_slice(wl_l, b, h)
+                cache.k_host[l, b, h, :P] = kk
+                cache.v_host[l, b, h, :P] = vv
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    sd = 1.0 / np.sqrt(H)
+
+    def rnd(*shape, scale=1.0):
+        return (torch.randn(*shape, generator=g, device=dev) * scale).to(torch.bfloat16)
+    xs = [rnd(B, 1, H) for _ in range(layers)]
+    wqs = [rnd(H, Hq * D, scale=sd) for _ in range(layers)]
+    wks = [rnd(H, Hkv * D, scale=sd) for _ in range(layers)]
+    wvs = [rnd(H, Hkv * D, scale=sd) for _ in range(layers)]
+    outs = [torch.empty((B, 1, Hq, D), dtype=torch.bfloat16, device=dev) for _ in range(layers)]
+    cache.set_lengths(np.full(B, P, np.int32))
+
+    def per_layer():
+        for l in range(layers):
+            cache.decode_layer(l, xs[l], wqs[l], wks[l], wvs[l], Hq, outs[l], stream)
+    cache.capture_step(xs, wqs, wks, wvs, Hq, outs)
+
+    def graph():
+        cache.launch_step(stream)
+    res = {}
+    for name, fn in (("per_layer_launches", per_layer), ("graph", graph)):
+        for _ in range(3):
+            fn()
+        res[name] = statistics.median(_time_once(torch, stream, flush, fn)
+                                      for _ in range(max(steps, 5)))
+    cache.sync(stream)
+    cache.free()
+    hb = layers * w.host_read_bytes()
+    best = min(res.values())
+    return {"layers": layers, "B": B, "P": P, "per_layer_host_bytes": w.host_read_bytes(),
+            "step_ms_per_layer_launches": res["per_layer_launches"],
+            "step_ms_graph": res["graph"], "tok_s_graph": B / (res["graph"] * 1e-3),
+            "host_link_gbs_graph": hb / (res["graph"] * 1e-3) / 1e9,
+            "frac_of_link_graph": hb / (res["graph"] * 1e-3) / 1e9 / link_rd,
+            "best_ms": best}
+
+
 def sweep(args, dkv, torch, dev, stream, flush, pk):
     """All workloads, one JSON line each (secondary measurements, not the headline)."""
     # link denominators over a 1 GiB mapped buffer
@@ -171,6 +226,8 @@ def sweep(args, dkv, torch, dev, stream, flush, pk):
             "frac_of_link": hb / (kern * 1e-3) / 1e9 / link_rd,
             "naive_zero_copy_ms": naive, "copy_to_hbm_then_attend_ms": staged_ms,
             "separate_kernels_ms": unfused_ms}), flush=True)
+    res = bench_multilayer(dkv, torch, dev, stream, flush, link_rd, args.steps)
+    print(json.dumps({"sweep": "multilayer_decode_step", "phase": "decode", **res}), flush=True)
     for name in ("llama8b_decode", "longctx_b1_s128k"):
         res = bench_paged_decode(wl.WORKLOADS[name], 16, dkv, torch, dev, stream, flush, link_rd,
                                  args.steps)
@@ -505,6 +562,9 @@ def main():
         # the same decode on a paged cache (16-token pages, shuffled page table)
         extras["paged_decode"] = bench_paged_decode(w, 16, dkv, torch, dev, stream, flush,
                                                     link_rd, args.steps)
+        # a 32-layer step of small per-layer caches: launches per layer vs one graph
+        extras["multilayer_decode_step"] = bench_multilayer(dkv, torch, dev, stream, flush,
+                                                            link_rd, args.steps)
 
     cpu = None
     if rank == 0 and not args.no_extras:

@@ -72,6 +72,7 @@ typedef struct {
     int page_tokens;        /* paged caches: rows per page; 0 for a dense cache */
     int num_pages;          /* paged caches: pages in each of the K and V pools */
     int max_pages_per_seq;  /* paged caches: page-table entries per sequence */
+    int layers;             /* layered caches: layers held (1 otherwise) */
 } dkv_cache_info_t;
 
 /* Allocate a K cache and a V cache of [batch][n_kv_heads][max_tokens][head_dim]
@@ -84,6 +85,19 @@ typedef struct {
  * memory), ALLOC. */
 dkv_status dkv_cache_alloc(dkv_cache** out, int batch, int n_kv_heads, int head_dim,
                            int max_tokens, dkv_dtype dtype);
+
+/* A layered cache: one pinned allocation each for K and V holding `layers`
+ * caches of [batch][n_kv_heads][max_tokens][head_dim] back to back, the
+ * (layers, batch, heads, tokens, head_dim) host tensor of a whole model
+ * ("DirectKV Guide: Zero-Copy KV Offloading on GH200 & GB200", Production
+ * Engineering Playbook (1)).  Layers share the sequence lengths: a token's
+ * calls go layer 0 .. layers-1 (dkv_decode_layer / dkv_prefill_layer), each
+ * appending at the current length, and the lengths advance with the call for
+ * the last layer.  dkv_decode / dkv_prefill refuse a layered cache
+ * (INVALID_ARG); the measurement baselines need a one-layer cache.
+ * Errors: as dkv_cache_alloc, plus INVALID_ARG for layers outside [1, 1024]. */
+dkv_status dkv_cache_alloc_layered(dkv_cache** out, int layers, int batch, int n_kv_heads,
+                                   int head_dim, int max_tokens, dkv_dtype dtype);
 
 /* A paged cache: K and V pools of [num_pages][n_kv_heads][page_tokens][head_dim]
  * elements each in pinned, mapped host memory, addressed through a per-
@@ -150,6 +164,34 @@ dkv_status dkv_cache_reserve(dkv_cache* cache, int n_q_heads, int max_new_tokens
 dkv_status dkv_decode(dkv_cache* cache, const void* x, const void* wq, const void* wk,
                       const void* wv, int hidden, int n_q_heads, void* out, void* stream);
 
+/* dkv_decode for one layer of a layered cache (layer 0 of any other cache):
+ * x, W and out are that layer's; the append goes to the layer's cache at the
+ * current length, and the lengths advance after the last layer.  Errors: as
+ * dkv_decode, plus INVALID_ARG for a layer outside [0, layers). */
+dkv_status dkv_decode_layer(dkv_cache* cache, int layer, const void* x, const void* wq,
+                            const void* wk, const void* wv, int hidden, int n_q_heads, void* out,
+                            void* stream);
+
+/* Capture one whole decode step (every layer in order, then the lengths
+ * advance by one) into a CUDA graph held by the cache, so that a step costs
+ * one graph launch instead of two launches per layer.  x, wq, wk, wv, out are
+ * host arrays of `layers` device pointers (as dkv_decode_layer takes them);
+ * the graph keeps those pointers and the kernel configuration chosen now, and
+ * reads the sequence lengths from device memory at run time, so every launch
+ * appends at the lengths of its own step.  Captures on a stream of the
+ * library's own; replaces an earlier capture.  Errors: as dkv_decode, CUDA
+ * (the capture or instantiation failed). */
+dkv_status dkv_step_graph_capture(dkv_cache* cache, int hidden, int n_q_heads,
+                                  const void* const* x, const void* const* wq,
+                                  const void* const* wk, const void* const* wv,
+                                  void* const* out);
+
+/* Launch the captured step on `stream`: checks capacity (CAPACITY if a
+ * sequence is full), publishes the host lengths to the device first if they
+ * changed outside graph steps (one synchronisation), then launches and
+ * advances the host lengths.  INVALID_ARG if nothing was captured. */
+dkv_status dkv_step_graph_launch(dkv_cache* cache, void* stream);
+
 /* One prefill (chunked-prefill) call: T new tokens per sequence at rows
  * [len[b], len[b]+T).  Query t of sequence b (absolute position len[b]+t)
  * attends causally to keys 0..len[b]+t.  Q = x.Wq is written to HBM first
@@ -162,6 +204,12 @@ dkv_status dkv_decode(dkv_cache* cache, const void* x, const void* wq, const voi
  * Errors as dkv_decode. */
 dkv_status dkv_prefill(dkv_cache* cache, const void* x, int T, const void* wq, const void* wk,
                        const void* wv, int hidden, int n_q_heads, void* out, void* stream);
+
+/* dkv_prefill for one layer of a layered cache (layer 0 of any other cache);
+ * the lengths advance by T after the last layer. */
+dkv_status dkv_prefill_layer(dkv_cache* cache, int layer, const void* x, int T, const void* wq,
+                             const void* wk, const void* wv, int hidden, int n_q_heads, void* out,
+                             void* stream);
 
 /* Synchronise the stream, then return and clear the device status word that
  * bounded waits write (DKV_ERR_TIMEOUT), or DKV_ERR_CUDA if the stream

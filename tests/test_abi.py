@@ -79,6 +79,14 @@ def test_invalid_arguments_fail_before_gpu_work(L):
     assert L.dkv_cache_alloc_paged(ctypes.byref(h), 1, 1, 96, 16, 4, 4, 0) == 2
     assert h.value is None
     assert L.dkv_cache_set_page_table(None, None) == 1
+    # layered caches and captured steps
+    assert L.dkv_cache_alloc_layered(ctypes.byref(h), 0, 1, 1, 128, 16, 0) == 1
+    assert L.dkv_cache_alloc_layered(ctypes.byref(h), 2, 0, 1, 128, 16, 0) == 1
+    assert h.value is None
+    assert L.dkv_decode_layer(None, 0, None, None, None, None, 64, 8, None, None) == 1
+    assert L.dkv_prefill_layer(None, 0, None, 4, None, None, None, 64, 8, None, None) == 1
+    assert L.dkv_step_graph_capture(None, 64, 8, None, None, None, None, None) == 1
+    assert L.dkv_step_graph_launch(None, None) == 1
 
 
 def test_binding_raises_typed_errors(L):

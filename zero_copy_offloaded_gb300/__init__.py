@@ -24,7 +24,8 @@ __all__ = [
     "dkv_last_error", "dkv_probe_read", "dkv_probe_write", "dkv_attend_naive",
     "dkv_decode_staged", "dkv_decode_unfused", "dkv_last_launch_count", "dkv_cache_kernel_timing",
     "dkv_cache_last_kernel_ms", "dkv_cache_alloc_paged", "dkv_cache_set_page_table",
-    "PagedKVCache",
+    "PagedKVCache", "LayeredKVCache", "dkv_cache_alloc_layered", "dkv_decode_layer",
+    "dkv_prefill_layer", "dkv_step_graph_capture", "dkv_step_graph_launch",
 ]
 
 BF16 = 0
@@ -55,7 +56,8 @@ class _CacheInfo(ctypes.Structure):
                 ("batch", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("max_tokens", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("page_tokens", ctypes.c_int),
-                ("num_pages", ctypes.c_int), ("max_pages_per_seq", ctypes.c_int)]
+                ("num_pages", ctypes.c_int), ("max_pages_per_seq", ctypes.c_int),
+                ("layers", ctypes.c_int)]
 
 
 _lib = None
@@ -79,6 +81,11 @@ def lib(build_if_missing: bool = False):
         "dkv_cache_alloc": [ctypes.POINTER(P), I, I, I, I, I],
         "dkv_cache_alloc_paged": [ctypes.POINTER(P), I, I, I, I, I, I, I],
         "dkv_cache_set_page_table": [P, P],
+        "dkv_cache_alloc_layered": [ctypes.POINTER(P), I, I, I, I, I, I],
+        "dkv_decode_layer": [P, I, P, P, P, P, I, I, P, P],
+        "dkv_prefill_layer": [P, I, P, I, P, P, P, I, I, P, P],
+        "dkv_step_graph_capture": [P, I, I, P, P, P, P, P],
+        "dkv_step_graph_launch": [P, P],
         "dkv_free": [P],
         "dkv_cache_host_ptrs": [P, ctypes.POINTER(P), ctypes.POINTER(P)],
         "dkv_cache_device_ptrs": [P, ctypes.POINTER(P), ctypes.POINTER(P)],
@@ -172,6 +179,40 @@ def dkv_cache_set_page_table(h, table):
     """table: int32 [batch, max_pages_per_seq] of pool page indices (-1: none)."""
     t = np.ascontiguousarray(table, dtype=np.int32)
     _check(lib().dkv_cache_set_page_table(h, t.ctypes.data), "dkv_cache_set_page_table")
+
+
+def dkv_cache_alloc_layered(layers, batch, n_kv_heads, head_dim, max_tokens, dtype="bf16") -> int:
+    h = ctypes.c_void_p()
+    _check(lib().dkv_cache_alloc_layered(ctypes.byref(h), layers, batch, n_kv_heads, head_dim,
+                                         max_tokens, _DTYPE[dtype]), "dkv_cache_alloc_layered")
+    return h.value
+
+
+def dkv_decode_layer(h, layer, x, wq, wk, wv, hidden, n_q_heads, out, stream=None):
+    _check(lib().dkv_decode_layer(h, layer, _ptr(x), _ptr(wq), _ptr(wk), _ptr(wv), hidden,
+                                  n_q_heads, _ptr(out), _stream(stream)), "dkv_decode_layer")
+
+
+def dkv_prefill_layer(h, layer, x, T, wq, wk, wv, hidden, n_q_heads, out, stream=None):
+    _check(lib().dkv_prefill_layer(h, layer, _ptr(x), T, _ptr(wq), _ptr(wk), _ptr(wv), hidden,
+                                   n_q_heads, _ptr(out), _stream(stream)), "dkv_prefill_layer")
+
+
+def _ptr_array(ts):
+    arr = (ctypes.c_void_p * len(ts))(*[_ptr(t) for t in ts])
+    return arr
+
+
+def dkv_step_graph_capture(h, hidden, n_q_heads, xs, wqs, wks, wvs, outs):
+    """Per-layer lists of device tensors; the arrays are copied into the graph."""
+    arrs = [_ptr_array(v) for v in (xs, wqs, wks, wvs, outs)]
+    _check(lib().dkv_step_graph_capture(h, hidden, n_q_heads,
+                                        *[ctypes.cast(a, ctypes.c_void_p) for a in arrs]),
+           "dkv_step_graph_capture")
+
+
+def dkv_step_graph_launch(h, stream=None):
+    _check(lib().dkv_step_graph_launch(h, _stream(stream)), "dkv_step_graph_launch")
 
 
 def dkv_free(h):
@@ -346,3 +387,31 @@ class PagedKVCache(KVCache):
     def set_page_table(self, table):
         dkv_cache_set_page_table(self.h, table)
         self.table = np.array(table, dtype=np.int32, copy=True)
+
+
+class LayeredKVCache(KVCache):
+    """A whole model's caches: numpy views [layers, B, Hkv, S_max, D] (uint16)
+    of the pinned K and V, per-layer decode / prefill and the captured step."""
+
+    def __init__(self, layers, batch, n_kv_heads, head_dim, max_tokens, dtype="bf16"):
+        self.L, self.B, self.Hkv, self.D, self.S_max = layers, batch, n_kv_heads, head_dim, max_tokens
+        self.dtype = dtype
+        self.h = dkv_cache_alloc_layered(layers, batch, n_kv_heads, head_dim, max_tokens, dtype)
+        kp, vp = dkv_cache_host_ptrs(self.h)
+        shape = (layers, batch, n_kv_heads, max_tokens, head_dim)
+        n = int(np.prod(shape))
+        self.k_host = np.ctypeslib.as_array((ctypes.c_uint16 * n).from_address(kp)).reshape(shape)
+        self.v_host = np.ctypeslib.as_array((ctypes.c_uint16 * n).from_address(vp)).reshape(shape)
+
+    def decode_layer(self, layer, x, wq, wk, wv, n_q_heads, out, stream=None):
+        dkv_decode_layer(self.h, layer, x, wq, wk, wv, x.shape[-1], n_q_heads, out, stream)
+
+    def prefill_layer(self, layer, x, wq, wk, wv, n_q_heads, out, stream=None):
+        dkv_prefill_layer(self.h, layer, x, x.shape[1], wq, wk, wv, x.shape[-1], n_q_heads, out,
+                          stream)
+
+    def capture_step(self, xs, wqs, wks, wvs, n_q_heads, outs):
+        dkv_step_graph_capture(self.h, xs[0].shape[-1], n_q_heads, xs, wqs, wks, wvs, outs)
+
+    def launch_step(self, stream=None):
+        dkv_step_graph_launch(self.h, stream)

@@ -30,6 +30,15 @@
 namespace dkv {
 namespace {
 
+// Cached rows of sequence b before this call's append.
+__device__ __forceinline__ int seq_len(const DecodeParams& p, int b) {
+  return p.len_dev ? __ldg(p.len_dev + b) : p.len[b];
+}
+
+__global__ void advance_lengths_kernel(int* len, int B, int T) {
+  if (threadIdx.x < B) len[threadIdx.x] += T;
+}
+
 constexpr int kConsumerWarps = 8;
 constexpr int kProducerWarps = 2;
 constexpr int kConsumers = kConsumerWarps * 32;
@@ -39,10 +48,20 @@ constexpr int kBarConsumers = 1;  // named barrier id for the consumer warps
 constexpr int kProjRows = 128;    // H rows per projection chunk
 constexpr int kProjCols = 64;     // columns per projection pass (multiple of 8)
 
+constexpr int kSmemCap = 232448 - 1024;  // dynamic shared memory per CTA, with margin
+
 // Shared-memory layout (byte offsets), all derived from the launch shape.
+// The projection's weight / x staging gets as many chunk stages (4 down to
+// 2) as fit beside the tile ring: the in-order FMA chains wait on one chunk
+// at a time, so deeper staging keeps more HBM loads in flight.
 struct DecodeSmem {
-  int ring, bars, q, s, alpha, ml, red, wproj, xproj, flag, total;
+  int ring, bars, q, s, alpha, ml, red, wproj, xproj, flag, total, proj_stages;
   __host__ __device__ DecodeSmem(int D, int G, int N, int stages, int B) {
+    for (proj_stages = 4; proj_stages > 2; --proj_stages)
+      if (layout(D, G, N, stages, B) <= kSmemCap) break;
+    layout(D, G, N, stages, B);
+  }
+  __host__ __device__ int layout(int D, int G, int N, int stages, int B) {
     int tile_bytes = N * D * 2;
     int off = 0;
     ring = off; off += stages * 2 * tile_bytes;
@@ -53,12 +72,21 @@ struct DecodeSmem {
     ml = off; off += 2 * G * 4;
     red = off; off += kConsumers * 2 * 4;
     off = (off + 15) & ~15;
-    wproj = off; off += 2 * kProjRows * kProjCols * 2;
-    xproj = off; off += 2 * B * kProjRows * 2;
+    wproj = off; off += proj_stages * kProjRows * kProjCols * 2;
+    xproj = off; off += proj_stages * B * kProjRows * 2;
     flag = off; off += 16;
     total = off;
+    return total;
   }
 };
+
+// cp.async.wait_group with the count known only at run time (2..4 stages).
+__device__ __forceinline__ void cp_async_wait_stages(int pending) {
+  if (pending >= 3) cp_async_wait_group<3>();
+  else if (pending == 2) cp_async_wait_group<2>();
+  else if (pending == 1) cp_async_wait_group<1>();
+  else cp_async_wait_group<0>();
+}
 
 template <typename T, int D>
 __device__ __forceinline__ const T* col_source(const DecodeParams& p, int col, int& which,
@@ -76,8 +104,9 @@ __device__ __forceinline__ const T* col_source(const DecodeParams& p, int col, i
 template <typename T, int D>
 __device__ void project_columns(const DecodeParams& p, int c_begin, int c_end, uint8_t* smem,
                                 const DecodeSmem& L, int ctid) {
-  T* wbuf = reinterpret_cast<T*>(smem + L.wproj);   // [2][kProjRows][kProjCols]
-  T* xbuf = reinterpret_cast<T*>(smem + L.xproj);   // [2][B][kProjRows]
+  T* wbuf = reinterpret_cast<T*>(smem + L.wproj);   // [S][kProjRows][kProjCols]
+  T* xbuf = reinterpret_cast<T*>(smem + L.xproj);   // [S][B][kProjRows]
+  const int S = L.proj_stages;
   const T* x = static_cast<const T*>(p.x);
   const int B = p.B, H = p.H;
   const int nchunks = (H + kProjRows - 1) / kProjRows;
@@ -94,6 +123,10 @@ __device__ void project_columns(const DecodeParams& p, int c_begin, int c_end, u
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 
       auto issue = [&](int chunk, int buf) {
+        if (chunk >= nchunks) {  // keep one (empty) group per chunk slot
+          cp_async_commit();
+          return;
+        }
         const int j0 = chunk * kProjRows;
         const int rows = min(kProjRows, H - j0);
         const int pieces_per_row = ncols / 8;
@@ -114,31 +147,45 @@ __device__ void project_columns(const DecodeParams& p, int c_begin, int c_end, u
         cp_async_commit();
       };
 
-      issue(0, 0);
+      for (int c = 0; c < S - 1; ++c) issue(c, c);
       for (int c = 0; c < nchunks; ++c) {
-        if (c + 1 < nchunks) {
-          issue(c + 1, (c + 1) & 1);
-          cp_async_wait_group<1>();
-        } else {
-          cp_async_wait_group<0>();
-        }
+        // chunk c + S - 1 goes into the slot chunk c - 1 used (every thread
+        // passed the barrier after reading it); chunk c is then complete once
+        // at most S - 1 newer groups are pending
+        issue(c + S - 1, (c + S - 1) % S);
+        cp_async_wait_stages(S - 1);
         named_bar_sync(kBarConsumers, kConsumers);
         if (active) {
           const int rows = min(kProjRows, H - c * kProjRows);
-          const T* wsrc = wbuf + (c & 1) * kProjRows * kProjCols;
-          const T* xs = xbuf + (c & 1) * B * kProjRows;
+          const T* wsrc = wbuf + (c % S) * kProjRows * kProjCols;
+          const T* xs = xbuf + (c % S) * B * kProjRows;
           const bool two = b0 + 1 < B;
-#pragma unroll 4
-          for (int j = 0; j < rows; ++j) {
-            const uint32_t w2 = *reinterpret_cast<const uint32_t*>(wsrc + j * kProjCols + pair * 2);
-            const float2 w = DT<T>::to_f2(w2);
-            const float xa = DT<T>::to_f(xs[b0 * kProjRows + j]);
-            acc[0] = fmaf(xa, w.x, acc[0]);
-            acc[1] = fmaf(xa, w.y, acc[1]);
-            if (two) {
-              const float xb = DT<T>::to_f(xs[(b0 + 1) * kProjRows + j]);
-              acc[2] = fmaf(xb, w.x, acc[2]);
-              acc[3] = fmaf(xb, w.y, acc[3]);
+          // 8 rows per step (rows is a multiple of 16): all loads of a step
+          // are issued before its FMA chains, which stay in row order
+#pragma unroll 2
+          for (int j = 0; j < rows; j += 8) {
+            uint32_t w8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              w8[k] = *reinterpret_cast<const uint32_t*>(wsrc + (j + k) * kProjCols + pair * 2);
+            const uint4 xa8 = *reinterpret_cast<const uint4*>(xs + b0 * kProjRows + j);
+            const uint4 xb8 =
+                two ? *reinterpret_cast<const uint4*>(xs + (b0 + 1) * kProjRows + j) : xa8;
+            const uint32_t xa4[4] = {xa8.x, xa8.y, xa8.z, xa8.w};
+            const uint32_t xb4[4] = {xb8.x, xb8.y, xb8.z, xb8.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float2 w = DT<T>::to_f2(w8[k]);
+              const float2 xa = DT<T>::to_f2(xa4[k / 2]);
+              const float xav = (k & 1) ? xa.y : xa.x;
+              acc[0] = fmaf(xav, w.x, acc[0]);
+              acc[1] = fmaf(xav, w.y, acc[1]);
+              if (two) {
+                const float2 xb = DT<T>::to_f2(xb4[k / 2]);
+                const float xbv = (k & 1) ? xb.y : xb.x;
+                acc[2] = fmaf(xbv, w.x, acc[2]);
+                acc[3] = fmaf(xbv, w.y, acc[3]);
+              }
             }
           }
         }
@@ -160,7 +207,7 @@ __device__ void project_columns(const DecodeParams& p, int c_begin, int c_end, u
             T* ws = static_cast<T*>(p.kv_ws) + ((size_t)b * 2 + (which - 1)) * p.Hkv * D + local;
             ws[0] = v0; ws[1] = v1;
             T* host = static_cast<T*>(which == 1 ? p.k_host : p.v_host) +
-                      p.lay.row(b, kvh, p.len[b], D) + d;
+                      p.lay.row(b, kvh, seq_len(p, b), D) + d;
             host[0] = v0; host[1] = v1;   // the append: one write across the link
           }
         }
@@ -179,7 +226,7 @@ __device__ __forceinline__ UnitRange unit_range(const DecodeParams& p, int u) {
   const int bh = u / p.splits;
   r.kvh = bh % p.Hkv;
   r.b = bh / p.Hkv;
-  r.S = p.len[r.b] + 1;  // keys after the append
+  r.S = seq_len(p, r.b) + 1;  // keys after the append
   const int nt = (r.S + p.tile_n - 1) / p.tile_n;
   r.t_lo = (int)((long long)r.split * nt / p.splits);
   r.t_hi = (int)((long long)(r.split + 1) * nt / p.splits);
@@ -220,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
       const T* vg = static_cast<const T*>(p.v_read);
       // rows read from the host: the cached ones (the fused path takes the new
       // row from HBM), or every row when the projection ran as its own launch
-      const int cached = p.len[r.b] + (p.mode == kDecodeAttendOnly ? 1 : 0);
+      const int cached = seq_len(p, r.b) + (p.mode == kDecodeAttendOnly ? 1 : 0);
       for (int t = r.t_lo; t < r.t_hi; ++t, ++it) {
         const int stage = it % stages;
         const uint32_t par = ((it / stages) & 1) ^ 1;
@@ -331,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
         }
       }
       // the new token's row (if in this tile) comes from the HBM workspace
-      const int rnew = p.len[r.b] - key0;
+      const int rnew = seq_len(p, r.b) - key0;
       if (p.mode == kDecodeFused && rnew >= 0 && rnew < N && ctid < 2 * CPR) {
         const int which = ctid / CPR, c = ctid % CPR;
         const T* src = static_cast<const T*>(p.kv_ws) +
@@ -479,10 +526,25 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, int smem, cudaStrea
   auto kern = decode_fused_kernel<T, D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  void* args[] = {const_cast<DecodeParams*>(&p)};
   timer.before(s);
-  e = cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(kThreads), args,
-                                  (size_t)smem, s);
+  if (p.len_dev) {
+    // the form a stream capture records as a cooperative graph node
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+  } else {
+    void* args[] = {const_cast<DecodeParams*>(&p)};
+    e = cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(kThreads), args,
+                                    (size_t)smem, s);
+  }
   if (e != cudaSuccess) return e;
   timer.after(s);
   if (p.mode == kDecodeProjectOnly) return cudaSuccess;
@@ -523,6 +585,11 @@ cudaError_t dispatch(int dtype, int D, int G, F&& f) {
 bool decode_supported(int dtype, int D, int G) {
   return (dtype == DKV_BF16 || dtype == DKV_FP16) && (D == 64 || D == 128) &&
          (G == 1 || G == 2 || G == 4 || G == 8);
+}
+
+cudaError_t launch_advance_lengths(int* len, int B, int T, cudaStream_t s) {
+  advance_lengths_kernel<<<1, 64, 0, s>>>(len, B, T);
+  return cudaGetLastError();
 }
 
 int decode_smem_bytes(int dtype, int D, int G, int tile_n, int stages, int B) {

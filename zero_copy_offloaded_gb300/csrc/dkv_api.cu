@@ -84,6 +84,15 @@ struct dkv_cache {
   int page_tokens, page_shift, num_pages, max_pages;
   std::vector<int32_t> pages;  // host copy of the page table [B][max_pages], -1 = none
   int* pages_dev;              // device copy read by the kernels
+  // layered caches: `layers` caches of layer_elems elements each for K and V
+  int layers;
+  size_t layer_elems;
+  // decode-step graphs read the lengths from len_dev; set when the host
+  // lengths changed outside a graph step (refreshed before the next one)
+  int* len_dev;
+  bool len_dev_stale;
+  cudaGraphExec_t step_exec;
+  cudaStream_t capture_stream;
   std::mutex mu;
 };
 
@@ -220,7 +229,7 @@ dkv_status set_device(dkv_cache* c) {
 dkv_status decode_impl(dkv_cache* c, const void* x, const void* wq, const void* wk,
                        const void* wv, int hidden, int n_q_heads, void* out,
                        const void* k_read, const void* v_read, cudaStream_t s,
-                       bool unfused = false) {
+                       bool unfused = false, int layer = 0, bool capture = false) {
   const int G = n_q_heads / c->Hkv;
   if (!decode_supported(c->dtype, c->D, G))
     return fail(DKV_ERR_UNSUPPORTED, "no decode kernel for dtype=%d D=%d G=%d", c->dtype, c->D, G);
@@ -238,8 +247,11 @@ dkv_status decode_impl(dkv_cache* c, const void* x, const void* wq, const void* 
   memset(&p, 0, sizeof p);
   char* w = static_cast<char*>(c->ws.base);
   p.x = x; p.wq = wq; p.wk = wk; p.wv = wv;
-  p.k_read = k_read; p.v_read = v_read;
-  p.k_host = c->k_dev; p.v_host = c->v_dev;
+  const size_t loff = (size_t)layer * c->layer_elems * 2;  // bytes
+  p.k_read = static_cast<const char*>(k_read) + loff;
+  p.v_read = static_cast<const char*>(v_read) + loff;
+  p.k_host = static_cast<char*>(c->k_dev) + loff;
+  p.v_host = static_cast<char*>(c->v_dev) + loff;
   p.q_ws = w; p.kv_ws = w + q_b;
   p.part_o = reinterpret_cast<float*>(w + q_b + kv_b);
   p.part_lse = reinterpret_cast<float*>(w + q_b + kv_b + po_b);
@@ -251,7 +263,8 @@ dkv_status decode_impl(dkv_cache* c, const void* x, const void* wq, const void* 
   p.debug_withhold = c->debug_withhold;
   p.lay = layout_of(c);
   fill_lens(p.len, c->len);
-  g_last_launches = 0;
+  if (capture) p.len_dev = c->len_dev;
+  if (!capture) g_last_launches = 0;
   cudaError_t e;
   if (unfused) {  // projection + append, then attention over host rows only
     p.mode = kDecodeProjectOnly;
@@ -260,16 +273,29 @@ dkv_status decode_impl(dkv_cache* c, const void* x, const void* wq, const void* 
     if (e == cudaSuccess)
       e = launch_decode(p, c->dtype, ch.grid, ch.smem, s, &g_last_launches, c->timer);
   } else {
-    e = launch_decode(p, c->dtype, ch.grid, ch.smem, s, &g_last_launches, c->timer);
+    e = launch_decode(p, c->dtype, ch.grid, ch.smem, s, &g_last_launches,
+                      capture ? KernelTimer() : c->timer);
   }
+  if (capture) return e == cudaSuccess ? DKV_OK : cuda_fail(e, "decode launch in a capture");
   c->timer_used = c->timer.start != nullptr;
   if (e != cudaSuccess) {
     cudaGetLastError();
     return cuda_fail(e, "decode launch");
   }
   c->last_stream = s;
-  for (int b = 0; b < B; ++b) c->len[b] += 1;
+  if (layer == c->layers - 1) {  // a token is complete once its last layer is
+    for (int b = 0; b < B; ++b) c->len[b] += 1;
+    c->len_dev_stale = true;
+  }
   return DKV_OK;
+}
+
+// Workspace bytes a decode call with G query heads per KV head needs.
+size_t decode_ws_bytes(const dkv_cache* c, int n_q_heads, int splits) {
+  const int B = c->B, D = c->D;
+  return align_up((size_t)B * n_q_heads * D * 2, 256) + align_up((size_t)B * 2 * c->Hkv * D * 2, 256) +
+         align_up((size_t)B * n_q_heads * splits * D * 4, 256) +
+         align_up((size_t)B * n_q_heads * splits * 4, 256);
 }
 
 }  // namespace
@@ -298,7 +324,7 @@ int dkv_last_launch_count(void) { return g_last_launches; }
 // elements each for K and for V in pinned, mapped host memory.
 static dkv_status alloc_common(dkv_cache** out, int batch, int n_kv_heads, int head_dim,
                                int max_tokens, dkv_dtype dtype, size_t rows, int page_tokens,
-                               int num_pages, int max_pages) {
+                               int num_pages, int max_pages, int layers = 1) {
   if (!out) return fail(DKV_ERR_INVALID_ARG, "null output handle");
   *out = nullptr;
   if (batch <= 0 || batch > kMaxBatch)
@@ -322,7 +348,7 @@ static dkv_status alloc_common(dkv_cache** out, int batch, int n_kv_heads, int h
   cudaDeviceGetAttribute(&can_map, cudaDevAttrCanMapHostMemory, dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (!can_map) return fail(DKV_ERR_NO_MAPPED_MEMORY, "device %d cannot map host memory", dev);
-  const size_t bytes = rows * head_dim * 2;
+  const size_t bytes = rows * head_dim * 2 * layers;
   void* kh = nullptr;
   void* vh = nullptr;
   e = cudaHostAlloc(&kh, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
@@ -366,6 +392,16 @@ static dkv_status alloc_common(dkv_cache** out, int batch, int n_kv_heads, int h
     }
     cudaMemset(pages_dev, 0xff, table * sizeof(int32_t));  // -1: no page
   }
+  int* len_dev = nullptr;
+  if ((e = cudaMalloc(&len_dev, kMaxBatch * sizeof(int))) != cudaSuccess) {
+    cudaGetLastError();
+    if (pages_dev) cudaFree(pages_dev);
+    cudaFree(st);
+    cudaFreeHost(kh);
+    cudaFreeHost(vh);
+    return fail(DKV_ERR_ALLOC, "lengths cudaMalloc: %s", cudaGetErrorString(e));
+  }
+  cudaMemset(len_dev, 0, kMaxBatch * sizeof(int));
   cudaMemset(st, 0, sizeof(DeviceStatus));
   cudaDeviceSynchronize();
   dkv_cache* c = new dkv_cache;
@@ -388,8 +424,29 @@ static dkv_status alloc_common(dkv_cache** out, int batch, int n_kv_heads, int h
   c->max_pages = max_pages;
   c->pages.assign(table, -1);
   c->pages_dev = pages_dev;
+  c->layers = layers;
+  c->layer_elems = rows * head_dim;
+  c->len_dev = len_dev;
+  c->len_dev_stale = false;
+  c->step_exec = nullptr;
+  c->capture_stream = nullptr;
   *out = c;
   return DKV_OK;
+}
+
+dkv_status dkv_cache_alloc_layered(dkv_cache** out, int layers, int batch, int n_kv_heads,
+                                   int head_dim, int max_tokens, dkv_dtype dtype) {
+  if (!out) return fail(DKV_ERR_INVALID_ARG, "null output handle");
+  *out = nullptr;
+  if (layers <= 0 || layers > 1024)
+    return fail(DKV_ERR_INVALID_ARG, "layers=%d must be in [1, 1024]", layers);
+  if (batch <= 0 || batch > kMaxBatch)
+    return fail(DKV_ERR_INVALID_ARG, "batch=%d must be in [1, %d]", batch, kMaxBatch);
+  if (n_kv_heads <= 0 || max_tokens <= 0)
+    return fail(DKV_ERR_INVALID_ARG, "n_kv_heads=%d and max_tokens=%d must be positive",
+                n_kv_heads, max_tokens);
+  return alloc_common(out, batch, n_kv_heads, head_dim, max_tokens, dtype,
+                      (size_t)batch * n_kv_heads * max_tokens, 0, 0, 0, layers);
 }
 
 dkv_status dkv_cache_alloc(dkv_cache** out, int batch, int n_kv_heads, int head_dim,
@@ -459,6 +516,12 @@ dkv_status dkv_free(dkv_cache* c) {
   cudaFree(c->status);
   if (c->pages_dev) cudaFree(c->pages_dev);
   c->pages_dev = nullptr;
+  if (c->len_dev) cudaFree(c->len_dev);
+  c->len_dev = nullptr;
+  if (c->step_exec) cudaGraphExecDestroy(c->step_exec);
+  c->step_exec = nullptr;
+  if (c->capture_stream) cudaStreamDestroy(c->capture_stream);
+  c->capture_stream = nullptr;
   cudaFreeHost(c->k_host);
   cudaFreeHost(c->v_host);
   // The handle memory is kept (tagged dead) so a second free is detected
@@ -491,6 +554,7 @@ dkv_status dkv_cache_set_lengths(dkv_cache* c, const int32_t* len) {
                   c->max_tokens);
   }
   for (int b = 0; b < c->B; ++b) c->len[b] = len[b];
+  c->len_dev_stale = true;
   return DKV_OK;
 }
 
@@ -502,7 +566,7 @@ dkv_status dkv_cache_get_lengths(const dkv_cache* c, int32_t* len) {
 
 dkv_status dkv_cache_info(const dkv_cache* c, dkv_cache_info_t* info) {
   if (!valid(c) || !info) return fail(DKV_ERR_INVALID_ARG, "invalid argument");
-  info->host_pinned_bytes = 2 * pool_rows(c) * c->D * 2;
+  info->host_pinned_bytes = 2 * pool_rows(c) * c->D * 2 * c->layers;
   info->device_workspace_bytes = c->ws.bytes + sizeof(DeviceStatus) +
                                  c->pages.size() * sizeof(int32_t);
   info->device_staging_bytes = 0;
@@ -510,6 +574,7 @@ dkv_status dkv_cache_info(const dkv_cache* c, dkv_cache_info_t* info) {
   info->max_tokens = c->max_tokens; info->dtype = c->dtype;
   info->page_tokens = c->page_tokens; info->num_pages = c->num_pages;
   info->max_pages_per_seq = c->max_pages;
+  info->layers = c->layers;
   return DKV_OK;
 }
 
@@ -554,20 +619,113 @@ dkv_status dkv_cache_reserve(dkv_cache* c, int n_q_heads, int max_new_tokens) {
   return ensure_ws(c, std::max(need, pre));
 }
 
-dkv_status dkv_decode(dkv_cache* c, const void* x, const void* wq, const void* wk,
-                      const void* wv, int hidden, int n_q_heads, void* out, void* stream) {
+dkv_status dkv_decode_layer(dkv_cache* c, int layer, const void* x, const void* wq,
+                            const void* wk, const void* wv, int hidden, int n_q_heads, void* out,
+                            void* stream) {
   dkv_status st = check_call(c, x, wq, wk, wv, hidden, n_q_heads, out, 1);
   if (st != DKV_OK) return st;
+  if (layer < 0 || layer >= c->layers)
+    return fail(DKV_ERR_INVALID_ARG, "layer %d outside [0, %d)", layer, c->layers);
   std::lock_guard<std::mutex> lk(c->mu);
   if ((st = set_device(c)) != DKV_OK) return st;
   return decode_impl(c, x, wq, wk, wv, hidden, n_q_heads, out, c->k_dev, c->v_dev,
-                     static_cast<cudaStream_t>(stream));
+                     static_cast<cudaStream_t>(stream), false, layer);
+}
+
+dkv_status dkv_decode(dkv_cache* c, const void* x, const void* wq, const void* wk,
+                      const void* wv, int hidden, int n_q_heads, void* out, void* stream) {
+  if (valid(c) && c->layers != 1)
+    return fail(DKV_ERR_INVALID_ARG, "a layered cache takes dkv_decode_layer");
+  return dkv_decode_layer(c, 0, x, wq, wk, wv, hidden, n_q_heads, out, stream);
+}
+
+dkv_status dkv_step_graph_capture(dkv_cache* c, int hidden, int n_q_heads,
+                                  const void* const* x, const void* const* wq,
+                                  const void* const* wk, const void* const* wv,
+                                  void* const* out) {
+  if (!valid(c) || !x || !wq || !wk || !wv || !out)
+    return fail(DKV_ERR_INVALID_ARG, "invalid argument");
+  for (int l = 0; l < c->layers; ++l) {
+    dkv_status st = check_call(c, x[l], wq[l], wk[l], wv[l], hidden, n_q_heads, out[l], 1);
+    if (st != DKV_OK) return st;
+  }
+  std::lock_guard<std::mutex> lk(c->mu);
+  dkv_status st = set_device(c);
+  if (st != DKV_OK) return st;
+  const int G = n_q_heads / c->Hkv;
+  if (!decode_supported(c->dtype, c->D, G))
+    return fail(DKV_ERR_UNSUPPORTED, "no decode kernel for dtype=%d D=%d G=%d", c->dtype, c->D, G);
+  DecodeChoice ch;
+  if ((st = choose_decode(c, G, &ch)) != DKV_OK) return st;
+  // everything a capture must not do: allocate, synchronise
+  if ((st = ensure_ws(c, decode_ws_bytes(c, n_q_heads, ch.splits))) != DKV_OK) return st;
+  cudaError_t e = cudaSuccess;
+  if (!c->capture_stream) e = cudaStreamCreateWithFlags(&c->capture_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(c->last_stream);
+  if (e != cudaSuccess) return cuda_fail(e, "capture stream");
+  if (c->step_exec) cudaGraphExecDestroy(c->step_exec);
+  c->step_exec = nullptr;
+  cudaStream_t cs = c->capture_stream;
+  e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamBeginCapture");
+  g_last_launches = 0;
+  for (int l = 0; l < c->layers && st == DKV_OK; ++l)
+    st = decode_impl(c, x[l], wq[l], wk[l], wv[l], hidden, n_q_heads, out[l], c->k_dev, c->v_dev,
+                     cs, false, l, true);
+  if (st == DKV_OK) {
+    e = launch_advance_lengths(c->len_dev, c->B, 1, cs);
+    if (e != cudaSuccess) st = cuda_fail(e, "length update in a capture");
+  }
+  cudaGraph_t graph = nullptr;
+  e = cudaStreamEndCapture(cs, &graph);
+  if (st != DKV_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    cudaGetLastError();
+    return st;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamEndCapture");
+  e = cudaGraphInstantiate(&c->step_exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) {
+    c->step_exec = nullptr;
+    return cuda_fail(e, "cudaGraphInstantiate");
+  }
+  c->len_dev_stale = true;  // written from the host lengths before the first launch
+  return DKV_OK;
+}
+
+dkv_status dkv_step_graph_launch(dkv_cache* c, void* stream) {
+  if (!valid(c)) return fail(DKV_ERR_INVALID_ARG, "invalid cache handle");
+  if (!c->step_exec) return fail(DKV_ERR_INVALID_ARG, "no decode step has been captured");
+  for (int b = 0; b < c->B; ++b)
+    if ((long)c->len[b] + 1 > c->max_tokens)
+      return fail(DKV_ERR_CAPACITY, "sequence %d: length %d + 1 > max_tokens %d", b, c->len[b],
+                  c->max_tokens);
+  std::lock_guard<std::mutex> lk(c->mu);
+  dkv_status st = set_device(c);
+  if (st != DKV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (c->len_dev_stale) {  // lengths changed outside graph steps: publish them first
+    e = cudaStreamSynchronize(c->last_stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(c->len_dev, c->len.data(), c->B * sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "lengths copy");
+    c->len_dev_stale = false;
+  }
+  e = cudaGraphLaunch(c->step_exec, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGraphLaunch");
+  c->last_stream = s;
+  for (int b = 0; b < c->B; ++b) c->len[b] += 1;
+  return DKV_OK;
 }
 
 dkv_status dkv_decode_unfused(dkv_cache* c, const void* x, const void* wq, const void* wk,
                               const void* wv, int hidden, int n_q_heads, void* out, void* stream) {
   dkv_status st = check_call(c, x, wq, wk, wv, hidden, n_q_heads, out, 1);
   if (st != DKV_OK) return st;
+  if (c->layers != 1) return fail(DKV_ERR_UNSUPPORTED, "unfused decode needs a one-layer cache");
   std::lock_guard<std::mutex> lk(c->mu);
   if ((st = set_device(c)) != DKV_OK) return st;
   return decode_impl(c, x, wq, wk, wv, hidden, n_q_heads, out, c->k_dev, c->v_dev,
@@ -580,7 +738,8 @@ dkv_status dkv_decode_staged(dkv_cache* c, const void* x, const void* wq, const 
   dkv_status st = check_call(c, x, wq, wk, wv, hidden, n_q_heads, out, 1);
   if (st != DKV_OK) return st;
   if (!k_stage || !v_stage) return fail(DKV_ERR_INVALID_ARG, "null staging buffer");
-  if (c->page_tokens) return fail(DKV_ERR_UNSUPPORTED, "staged decode needs a dense cache");
+  if (c->page_tokens || c->layers != 1)
+    return fail(DKV_ERR_UNSUPPORTED, "staged decode needs a dense one-layer cache");
   std::lock_guard<std::mutex> lk(c->mu);
   if ((st = set_device(c)) != DKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -601,10 +760,13 @@ dkv_status dkv_decode_staged(dkv_cache* c, const void* x, const void* wq, const 
   return decode_impl(c, x, wq, wk, wv, hidden, n_q_heads, out, k_stage, v_stage, s);
 }
 
-dkv_status dkv_prefill(dkv_cache* c, const void* x, int T, const void* wq, const void* wk,
-                       const void* wv, int hidden, int n_q_heads, void* out, void* stream) {
+dkv_status dkv_prefill_layer(dkv_cache* c, int layer, const void* x, int T, const void* wq,
+                             const void* wk, const void* wv, int hidden, int n_q_heads, void* out,
+                             void* stream) {
   dkv_status st = check_call(c, x, wq, wk, wv, hidden, n_q_heads, out, T);
   if (st != DKV_OK) return st;
+  if (layer < 0 || layer >= c->layers)
+    return fail(DKV_ERR_INVALID_ARG, "layer %d outside [0, %d)", layer, c->layers);
   std::lock_guard<std::mutex> lk(c->mu);
   if ((st = set_device(c)) != DKV_OK) return st;
   const int G = n_q_heads / c->Hkv;
@@ -625,7 +787,11 @@ dkv_status dkv_prefill(dkv_cache* c, const void* x, int T, const void* wq, const
   PrefillParams p;
   memset(&p, 0, sizeof p);
   p.x = x; p.wk = wk; p.wv = wv; p.q = w;
-  p.k_read = c->k_dev; p.v_read = c->v_dev; p.k_host = c->k_dev; p.v_host = c->v_dev;
+  const size_t loff = (size_t)layer * c->layer_elems * 2;  // bytes
+  p.k_read = static_cast<char*>(c->k_dev) + loff;
+  p.v_read = static_cast<char*>(c->v_dev) + loff;
+  p.k_host = static_cast<char*>(c->k_dev) + loff;
+  p.v_host = static_cast<char*>(c->v_dev) + loff;
   p.part_o = w + q_b;
   p.part_lse = reinterpret_cast<float*>(w + q_b + po_b);
   p.part_k = reinterpret_cast<int*>(w + q_b + po_b + pl_b);
@@ -645,8 +811,18 @@ dkv_status dkv_prefill(dkv_cache* c, const void* x, int T, const void* wq, const
     return cuda_fail(e, "prefill launch");
   }
   c->last_stream = s;
-  for (int b = 0; b < B; ++b) c->len[b] += T;
+  if (layer == c->layers - 1) {  // the tokens are complete once their last layer is
+    for (int b = 0; b < B; ++b) c->len[b] += T;
+    c->len_dev_stale = true;
+  }
   return DKV_OK;
+}
+
+dkv_status dkv_prefill(dkv_cache* c, const void* x, int T, const void* wq, const void* wk,
+                       const void* wv, int hidden, int n_q_heads, void* out, void* stream) {
+  if (valid(c) && c->layers != 1)
+    return fail(DKV_ERR_INVALID_ARG, "a layered cache takes dkv_prefill_layer");
+  return dkv_prefill_layer(c, 0, x, T, wq, wk, wv, hidden, n_q_heads, out, stream);
 }
 
 dkv_status dkv_cache_kernel_timing(dkv_cache* c, int enable) {
@@ -727,7 +903,8 @@ dkv_status dkv_probe_write(void* dst, size_t bytes, void* stream) {
 dkv_status dkv_attend_naive(dkv_cache* c, const void* q, int n_q_heads, void* out, void* stream) {
   if (!valid(c) || !q || !out || n_q_heads <= 0 || n_q_heads % c->Hkv)
     return fail(DKV_ERR_INVALID_ARG, "invalid argument");
-  if (c->page_tokens) return fail(DKV_ERR_UNSUPPORTED, "naive attention needs a dense cache");
+  if (c->page_tokens || c->layers != 1)
+    return fail(DKV_ERR_UNSUPPORTED, "naive attention needs a dense one-layer cache");
   std::lock_guard<std::mutex> lk(c->mu);
   dkv_status st = set_device(c);
   if (st != DKV_OK) return st;
