@@ -9,6 +9,10 @@ method) serves both.
 Parity status (each function's pins live in ``tests/test_oracle.py``):
   round_bits  pinned: brute-force nearest-by-enumeration, ties, overflow,
               subnormals, numpy float16
+  decode_e4m3, round_e4m3
+              pinned: all 256 codes against the format's fields; nearest by
+              enumeration of the finite codes, ties to even, saturation
+  project_f32 pinned: the pure-Python fp32 sequential loop (bit-exact)
   project     pinned: pure-Python fp32 sequential loop (bit-exact) and the
               exact rational sum (within 1 ulp)
   attend      pinned: pure-Python per-element softmax, closed forms (Q=0 gives
@@ -20,5 +24,5 @@ Parity status (each function's pins live in ``tests/test_oracle.py``):
 """
 from .reference import (  # noqa: F401
     BF16, FP16, build, lib, decode_bits, round_bits, project, attend, step,
-    set_threads, max_threads,
+    set_threads, max_threads, project_f32, decode_e4m3, round_e4m3,
 )

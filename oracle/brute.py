@@ -80,6 +80,49 @@ def nearest_bits(v, dtype) -> int:
     return sign | (lo_bits if lo_bits % 2 == 0 else hi_bits)
 
 
+def e4m3_value(bits: int):
+    """Exact value of an 8-bit E4M3 pattern (1 sign, 4 exponent bits with bias
+    7, 3 mantissa bits; no infinities; exponent and mantissa all ones is NaN)."""
+    s = -1 if bits & 0x80 else 1
+    e = (bits >> 3) & 15
+    m = bits & 7
+    if e == 15 and m == 7:
+        return math.nan
+    if e == 0:
+        return s * Fraction(m, 8) * Fraction(2) ** -6
+    return s * (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+
+
+def e4m3_nearest(v) -> int:
+    """Nearest E4M3 pattern by enumeration of the finite codes; ties go to the
+    even mantissa; magnitudes past the largest finite value saturate to it."""
+    x = Fraction(v)
+    neg = x < 0 or (x == 0 and math.copysign(1.0, float(v)) < 0)
+    a = abs(x)
+    best = None
+    for bits in range(0, 0x7F):  # non-negative finite codes
+        d = abs(e4m3_value(bits) - a)
+        if best is None or d < best[0] or (d == best[0] and bits % 2 == 0):
+            best = (d, bits)
+    top = 0x7E  # 448
+    bits = top if a > e4m3_value(top) else best[1]
+    return (0x80 | bits) if neg else bits
+
+
+def f32_sums_seq(x_bits, w_bits, dtype):
+    """x [H] bits, w [H][N] bits -> [N] floats: the fp32 sequential sums (unrounded)."""
+    H = len(x_bits)
+    N = len(w_bits[0])
+    out = []
+    for c in range(N):
+        acc = 0.0
+        for j in range(H):
+            p = float(value_of(x_bits[j], dtype)) * float(value_of(w_bits[j][c], dtype))
+            acc = f32(acc + p)
+        out.append(acc)
+    return out
+
+
 def f32(x) -> float:
     """Round a Python float to the nearest IEEE single (ties to even)."""
     return struct.unpack("<f", struct.pack("<f", x))[0]

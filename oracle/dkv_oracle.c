@@ -15,6 +15,7 @@
  * itself with no tiling, splitting or online rescaling:
  *
  *   dkv_oracle_round     round a real value to bf16/fp16, nearest, ties to even
+ *   dkv_oracle_round_e4m3  the same to 8-bit E4M3, saturating (FP8 caches)
  *   dkv_oracle_project   projection: fp32 products (exact for 16-bit inputs)
  *                        accumulated in fp32 in sequential order j = 0..H-1,
  *                        then rounded to the storage dtype; also the fp64 sum
@@ -93,6 +94,52 @@ static uint16_t orc_encode(double v, int dt) {
     return sign | (uint16_t)(efield << mbits) | (uint16_t)(sig - (1u << mbits));
 }
 
+/* ---- 8-bit E4M3 (OCP 8-bit floating point, E4M3 variant) --------------
+ * 1 sign, 4 exponent (bias 7) and 3 mantissa bits; no infinities; exponent
+ * and mantissa all ones is NaN, so the largest finite value is 1.75 * 2^8 =
+ * 448; exponent 0 holds the subnormals m * 2^-9.  Used for the FP8 K/V cache
+ * format (unscaled). */
+
+static double orc_e4m3_decode(uint8_t b) {
+    int sign = (b >> 7) & 1, e = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (e == 15 && m == 7) v = NAN;
+    else if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp((double)(m + 8), e - 10);
+    return sign ? -v : v;
+}
+
+/* Nearest E4M3 value, ties to even, saturating at +-448 ("satfinite"): the
+ * same quantum construction as orc_encode with 3 mantissa bits and the
+ * smallest normal exponent -6; a result past 448 is clamped to 448. */
+static uint8_t orc_e4m3_encode(double v) {
+    const int mbits = 3, bias = 7, emin = -6;
+    uint8_t sign = signbit(v) ? 0x80u : 0u;
+    if (isnan(v)) return 0x7Fu;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    int E;
+    (void)frexp(a, &E);
+    int lead = E - 1;
+    if (lead < emin) lead = emin;
+    double r = nearbyint(a / ldexp(1.0, lead - mbits)) * ldexp(1.0, lead - mbits);
+    if (r > 448.0 || isinf(a)) r = 448.0;
+    if (r == 0.0) return sign;
+    (void)frexp(r, &E);
+    lead = E - 1;
+    if (lead < emin) return sign | (uint8_t)ldexp(r, mbits - emin); /* subnormal */
+    uint32_t sig = (uint32_t)ldexp(r, mbits - lead); /* in [8, 16) */
+    return sign | (uint8_t)((uint32_t)(lead + bias) << mbits) | (uint8_t)(sig - 8u);
+}
+
+void dkv_oracle_decode_e4m3(const uint8_t* bits, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_decode(bits[i]);
+}
+
+void dkv_oracle_round_e4m3(const double* v, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_encode(v[i]);
+}
+
 void dkv_oracle_set_threads(int n) {
 #ifdef _OPENMP
     if (n > 0) omp_set_num_threads(n);
@@ -120,10 +167,12 @@ void dkv_oracle_round(const double* v, int64_t n, int dt, uint16_t* out) {
 /* Projection Y = X . W for X [rows, H] and W [H, ncols] (16-bit bits,
  * row-major).  Each output accumulates the exact fp32 products
  * x[r][j] * w[j][c] in fp32, j = 0, 1, ..., H-1 in that order, starting from
- * +0; the sum is rounded once to the storage dtype (out_bits).  If
- * out_exact is non-null it receives the same sum taken in fp64 (diagnostic). */
+ * +0; the sum is rounded once to the storage dtype (out_bits, if non-null).
+ * out_f32, if non-null, receives the fp32 sum itself (before that rounding,
+ * for other storage formats); out_exact the same sum taken in fp64
+ * (diagnostic). */
 void dkv_oracle_project(const uint16_t* x, int rows, int H, const uint16_t* w, int ncols,
-                        int dt, uint16_t* out_bits, double* out_exact) {
+                        int dt, uint16_t* out_bits, double* out_exact, double* out_f32) {
     float* wf = (float*)malloc(sizeof(float) * (size_t)H * (size_t)ncols);
     for (int64_t i = 0; i < (int64_t)H * ncols; ++i) wf[i] = (float)orc_decode(w[i], dt);
 #pragma omp parallel for schedule(dynamic, 1)
@@ -142,7 +191,10 @@ void dkv_oracle_project(const uint16_t* x, int rows, int H, const uint16_t* w, i
             if (accd)
                 for (int c = 0; c < ncols; ++c) accd[c] += (double)xv * (double)wr[c];
         }
-        for (int c = 0; c < ncols; ++c) out_bits[(size_t)r * ncols + c] = orc_encode((double)acc[c], dt);
+        for (int c = 0; c < ncols; ++c) {
+            if (out_bits) out_bits[(size_t)r * ncols + c] = orc_encode((double)acc[c], dt);
+            if (out_f32) out_f32[(size_t)r * ncols + c] = (double)acc[c];
+        }
         if (accd) {
             memcpy(out_exact + (size_t)r * ncols, accd, sizeof(double) * (size_t)ncols);
             free(accd);

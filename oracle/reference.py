@@ -55,7 +55,9 @@ def lib():
             L.dkv_oracle_decode.argtypes = [P, ctypes.c_int64, ctypes.c_int, P]
             L.dkv_oracle_round.argtypes = [P, ctypes.c_int64, ctypes.c_int, P]
             L.dkv_oracle_project.argtypes = [P, ctypes.c_int, ctypes.c_int, P, ctypes.c_int,
-                                             ctypes.c_int, P, P]
+                                             ctypes.c_int, P, P, P]
+            L.dkv_oracle_decode_e4m3.argtypes = [P, ctypes.c_int64, P]
+            L.dkv_oracle_round_e4m3.argtypes = [P, ctypes.c_int64, P]
             L.dkv_oracle_attend.argtypes = [ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int, P, P,
                                             P, P, P]
             L.dkv_oracle_attend.restype = ctypes.c_int
@@ -105,8 +107,38 @@ def project(x_bits: np.ndarray, w_bits: np.ndarray, dtype, exact: bool = False):
     assert H == H2
     out = np.empty((rows, N), np.uint16)
     ex = np.empty((rows, N), np.float64) if exact else None
-    lib().dkv_oracle_project(_p(x), rows, H, _p(w), N, _DT[dtype], _p(out), _p(ex))
+    lib().dkv_oracle_project(_p(x), rows, H, _p(w), N, _DT[dtype], _p(out), _p(ex), None)
     return (out, ex) if exact else out
+
+
+def project_f32(x_bits: np.ndarray, w_bits: np.ndarray, dtype) -> np.ndarray:
+    """The fp32 sequential sums of project() before their rounding (float64 holding
+    fp32 values), for storage formats other than the inputs' dtype."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    rows, H = x.shape
+    H2, N = w.shape
+    assert H == H2
+    f = np.empty((rows, N), np.float64)
+    lib().dkv_oracle_project(_p(x), rows, H, _p(w), N, _DT[dtype], None, None, _p(f))
+    return f
+
+
+def decode_e4m3(bits: np.ndarray) -> np.ndarray:
+    """uint8 E4M3 bits -> exact float64 values (NaN for the NaN codes)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint8)
+    out = np.empty(b.shape, np.float64)
+    lib().dkv_oracle_decode_e4m3(_p(b), b.size, _p(out))
+    return out
+
+
+def round_e4m3(v: np.ndarray) -> np.ndarray:
+    """float64 values -> uint8 bits of the nearest E4M3 value (ties to even),
+    saturating at +-448."""
+    a = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(a.shape, np.uint8)
+    lib().dkv_oracle_round_e4m3(_p(a), a.size, _p(out))
+    return out
 
 
 def attend(K: np.ndarray, V: np.ndarray, Q: np.ndarray, pos, want_lse=False, want_weights=False):
@@ -131,8 +163,11 @@ def attend(K: np.ndarray, V: np.ndarray, Q: np.ndarray, pos, want_lse=False, wan
     return res[0] if len(res) == 1 else tuple(res)
 
 
-def step(x, wq, wk, wv, k_cache, v_cache, P, n_q_heads, dtype, rows=None):
+def step(x, wq, wk, wv, k_cache, v_cache, P, n_q_heads, dtype, rows=None, kv_format=None):
     """One decode/prefill call of the method, on the oracle.
+
+    kv_format "e4m3": the caches hold 8-bit E4M3 bits (uint8) and the new K/V
+    rows are the fp32 sums rounded once to E4M3; q stays in dtype.
 
     x [B,T,H] bits; wq [H,Hq*D]; wk, wv [H,Hkv*D]; k_cache, v_cache
     [B,Hkv,S_max,D] bits with rows [0,P) filled (P an int or per-sequence
@@ -149,8 +184,17 @@ def step(x, wq, wk, wv, k_cache, v_cache, P, n_q_heads, dtype, rows=None):
     Ps = np.broadcast_to(np.asarray(P, np.int64), (B,))
     xr = x.reshape(B * T, H)
     q = project(xr, wq, dtype).reshape(B, T, Hq, D)
-    k_new = project(xr, wk, dtype).reshape(B, T, Hkv, D)
-    v_new = project(xr, wv, dtype).reshape(B, T, Hkv, D)
+    fp8 = kv_format == "e4m3"
+    if fp8:
+        k_new = round_e4m3(project_f32(xr, wk, dtype)).reshape(B, T, Hkv, D)
+        v_new = round_e4m3(project_f32(xr, wv, dtype)).reshape(B, T, Hkv, D)
+        kv_decode = decode_e4m3
+    else:
+        k_new = project(xr, wk, dtype).reshape(B, T, Hkv, D)
+        v_new = project(xr, wv, dtype).reshape(B, T, Hkv, D)
+
+        def kv_decode(bits):
+            return decode_bits(bits, dtype)
     kc = k_cache.copy()
     vc = v_cache.copy()
     for b in range(B):
@@ -167,8 +211,8 @@ def step(x, wq, wk, wv, k_cache, v_cache, P, n_q_heads, dtype, rows=None):
     for b, ts in by_b.items():
         p = int(Ps[b])
         for kvh in range(Hkv):
-            Kf = decode_bits(kc[b, kvh, : p + T], dtype)
-            Vf = decode_bits(vc[b, kvh, : p + T], dtype)
+            Kf = kv_decode(kc[b, kvh, : p + T])
+            Vf = kv_decode(vc[b, kvh, : p + T])
             heads = list(range(kvh * G, (kvh + 1) * G))
             Qr = decode_bits(q[b][np.ix_(ts, heads)], dtype).reshape(-1, D)
             pos = np.repeat(np.asarray([p + t for t in ts], np.int32), G)

@@ -77,6 +77,66 @@ def test_round_matches_library_routines():
     assert np.array_equal(oracle.round_bits(f32.astype(np.float64), "bf16"), tb)
 
 
+def test_e4m3_decode_all_codes():
+    bits = np.arange(256, dtype=np.uint8)
+    got = oracle.decode_e4m3(bits)
+    for b in range(256):
+        ref = brute.e4m3_value(b)
+        if isinstance(ref, float) and math.isnan(ref):
+            assert math.isnan(got[b]), b
+        else:
+            assert got[b] == float(ref), b
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x38] == 1.0
+
+
+def test_e4m3_round_vs_enumeration():
+    rng = np.random.default_rng(17)
+    vals = list(rng.standard_normal(400) * 2.0 ** rng.integers(-12, 10, 400))
+    for b in range(0, 0x7E):  # every midpoint between neighbouring finite codes: ties
+        lo, hi = brute.e4m3_value(b), brute.e4m3_value(b + 1)
+        vals += [float((lo + hi) / 2), -float((lo + hi) / 2)]
+    vals += [0.0, -0.0, 448.0, 447.9, 460.0, 464.0, 465.0, 1e6, -1e6, 2.0 ** -10, 2.0 ** -11]
+    v = np.array(vals, np.float64)
+    got = oracle.round_e4m3(v)
+    assert list(got) == [brute.e4m3_nearest(float(x)) for x in v]
+
+
+def test_project_f32_vs_bruteforce():
+    rng = np.random.default_rng(23)
+    H, N = 29, 4
+    x = wl.to_bits(rng.standard_normal((2, H)).astype(np.float32), "bf16")
+    w = wl.to_bits((rng.standard_normal((H, N)) / 5).astype(np.float32), "bf16")
+    got = oracle.project_f32(x, w, "bf16")
+    for r in range(2):
+        ref = brute.f32_sums_seq(list(map(int, x[r])), [list(map(int, row)) for row in w], "bf16")
+        assert list(got[r]) == ref
+    # rounding the sums to the storage dtype is project() itself
+    assert np.array_equal(oracle.round_bits(got, "bf16"), oracle.project(x, w, "bf16"))
+
+
+def test_step_e4m3_cache():
+    """With E4M3 caches the appended rows are the fp32 sums rounded to E4M3, and
+    the attention runs over the decoded E4M3 values (checked against a step
+    over the same values held in fp64 by hand)."""
+    w = wl.Workload("t", "decode", B=1, H=32, Hq=4, Hkv=2, D=8, P=5, seed=3)
+    d = wl.make_dense(w)
+    rng = np.random.default_rng(4)
+    kc = oracle.round_e4m3(rng.standard_normal((1, 2, 8, 8)))
+    vc = oracle.round_e4m3(rng.standard_normal((1, 2, 8, 8)))
+    ref = oracle.step(d["x"], d["wq"], d["wk"], d["wv"], kc, vc, 5, 4, "bf16", kv_format="e4m3")
+    xr = d["x"].reshape(1, 32)
+    kn = oracle.round_e4m3(oracle.project_f32(xr, d["wk"], "bf16")).reshape(2, 8)
+    assert np.array_equal(ref["k_new"][0, 0], kn)
+    assert np.array_equal(ref["k_cache_after"][0, :, 5], kn)
+    q = oracle.decode_bits(oracle.project(xr, d["wq"], "bf16"), "bf16").reshape(4, 8)
+    K = oracle.decode_e4m3(ref["k_cache_after"][0])
+    V = oracle.decode_e4m3(ref["v_cache_after"][0])
+    for h in range(4):
+        o, _ = brute.attend([list(r) for r in K[h // 2, :6]], [list(r) for r in V[h // 2, :6]],
+                            list(q[h]), 6)
+        np.testing.assert_allclose(ref["out"][0, 0, h], o, rtol=0, atol=1e-12)
+
+
 # -------------------------------------------------------------- projection --
 
 def test_project_golden():
