@@ -57,6 +57,43 @@ def parse():
     return ap.parse_args()
 
 
+def bench_fp8_decode(w, dkv, torch, dev, stream, flush, link_rd, steps):
+    """The decode workload on an 8-bit E4M3 cache (the same values, converted
+    with torch's float8 type as input construction): half the host bytes."""
+    tdt = torch.bfloat16
+    cache = dkv.KVCache(w.B, w.Hkv, w.D, w.S_max, w.dtype, kv_format="e4m3")
+    for b in range(w.B):
+        for h in range(w.Hkv):
+            kk, vv = wl.cache_slice(w, b, h)
+            for host, bits in ((cache.k_host, kk), (cache.v_host, vv)):
+                f = torch.from_numpy(wl.bits_to_f32(bits, w.dtype)).to(torch.float8_e4m3fn)
+                host[b, h, :w.P] = f.view(torch.uint8).numpy()
+    dense = wl.make_dense(w)
+    x, wq, wk, wv = (torch.from_numpy(dense[k].view(np.int16)).view(tdt).to(dev)
+                     for k in ("x", "wq", "wk", "wv"))
+    x = x.reshape(w.B, 1, w.H)
+    out = torch.empty((w.B, 1, w.Hq, w.D), dtype=tdt, device=dev)
+    lens = np.full(w.B, w.P, np.int32)
+    dkv.dkv_cache_kernel_timing(cache.h, True)
+
+    def step():
+        cache.set_lengths(lens)
+        cache.decode(x, wq, wk, wv, w.Hq, out, stream)
+    for _ in range(3):
+        step()
+    ms, kern = [], []
+    for _ in range(max(steps, 5)):
+        ms.append(_time_once(torch, stream, flush, step))
+        kern.append(dkv.dkv_cache_last_kernel_ms(cache.h))
+    cache.free()
+    step_ms, kern_ms = statistics.median(ms), statistics.median(kern)
+    hb = w.host_read_bytes() // 2  # one byte per element
+    gbs = hb / (kern_ms * 1e-3) / 1e9
+    return {"workload": w.name, "kv_format": "e4m3", "host_read_bytes": hb, "step_ms": step_ms,
+            "tok_s": w.B / (step_ms * 1e-3), "fused_kernel_ms": kern_ms,
+            "host_link_gbs": gbs, "frac_of_link": gbs / link_rd}
+
+
 def bench_paged_decode(w, page_tokens, dkv, torch, dev, stream, flush, link_rd, steps):
     """The decode workload on a paged cache: pages of `page_tokens` rows, each
     sequence's pages drawn by a seeded permutation of the pool (no two
@@ -226,6 +263,10 @@ def sweep(args, dkv, torch, dev, stream, flush, pk):
             "frac_of_link": hb / (kern * 1e-3) / 1e9 / link_rd,
             "naive_zero_copy_ms": naive, "copy_to_hbm_then_attend_ms": staged_ms,
             "separate_kernels_ms": unfused_ms}), flush=True)
+    for name in ("llama8b_decode", "longctx_b1_s128k"):
+        res = bench_fp8_decode(wl.WORKLOADS[name], dkv, torch, dev, stream, flush, link_rd,
+                               args.steps)
+        print(json.dumps({"sweep": name + "_e4m3", "phase": "decode", **res}), flush=True)
     res = bench_multilayer(dkv, torch, dev, stream, flush, link_rd, args.steps)
     print(json.dumps({"sweep": "multilayer_decode_step", "phase": "decode", **res}), flush=True)
     for name in ("llama8b_decode", "longctx_b1_s128k"):
@@ -562,6 +603,9 @@ def main():
         # the same decode on a paged cache (16-token pages, shuffled page table)
         extras["paged_decode"] = bench_paged_decode(w, 16, dkv, torch, dev, stream, flush,
                                                     link_rd, args.steps)
+        # the same decode on an 8-bit E4M3 cache (half the host bytes)
+        extras["fp8_decode"] = bench_fp8_decode(w, dkv, torch, dev, stream, flush, link_rd,
+                                                args.steps)
         # a 32-layer step of small per-layer caches: launches per layer vs one graph
         extras["multilayer_decode_step"] = bench_multilayer(dkv, torch, dev, stream, flush,
                                                             link_rd, args.steps)

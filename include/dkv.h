@@ -62,6 +62,27 @@ typedef enum { DKV_BF16 = 0, DKV_FP16 = 1 } dkv_dtype;
 
 typedef struct dkv_cache dkv_cache; /* opaque; tagged so a stale handle is rejected */
 
+/* What the cache stores per K/V element: the dtype itself (2 bytes), or 8-bit
+ * E4M3 (OCP 8-bit floating point; 1 sign, 4 exponent, 3 mantissa bits; no
+ * infinities; largest finite 448), unscaled and saturating.  E4M3 halves the
+ * bytes the attention reads across the host link (the FP8 KV cache that
+ * "KV Offloading and Transfer" lists among the cheaper things to do first,
+ * in section 6, When it's worth it; not part of DirectKV's pages).  New
+ * rows are the fp32 projection sums rounded once to E4M3 (to nearest, ties
+ * to even, saturating); decode only, bf16 activations only. */
+typedef enum { DKV_KV_NATIVE = 0, DKV_KV_E4M3 = 1 } dkv_kv_format;
+
+/* Everything a cache can be: dense (page_tokens 0), paged (page_tokens > 0,
+ * one layer), layered (layers > 1, dense), in either element format.
+ * layers 0 counts as 1. */
+typedef struct {
+    int batch, n_kv_heads, head_dim, max_tokens;
+    dkv_dtype dtype;
+    dkv_kv_format kv_format;
+    int layers;
+    int page_tokens, num_pages, max_pages_per_seq;
+} dkv_cache_desc_t;
+
 /* Sizes of what a cache holds (the pages' memory accounting: zero bytes of
  * HBM staging; "Paper Notes: DirectKV", Experiments, GPU memory). */
 typedef struct {
@@ -73,6 +94,7 @@ typedef struct {
     int num_pages;          /* paged caches: pages in each of the K and V pools */
     int max_pages_per_seq;  /* paged caches: page-table entries per sequence */
     int layers;             /* layered caches: layers held (1 otherwise) */
+    int kv_format;          /* dkv_kv_format of the K/V elements */
 } dkv_cache_info_t;
 
 /* Allocate a K cache and a V cache of [batch][n_kv_heads][max_tokens][head_dim]
@@ -85,6 +107,15 @@ typedef struct {
  * memory), ALLOC. */
 dkv_status dkv_cache_alloc(dkv_cache** out, int batch, int n_kv_heads, int head_dim,
                            int max_tokens, dkv_dtype dtype);
+
+/* The general allocator behind dkv_cache_alloc, dkv_cache_alloc_layered and
+ * dkv_cache_alloc_paged, which also takes the element format.  An E4M3 cache
+ * serves dkv_decode / dkv_decode_layer / dkv_decode_unfused / captured steps
+ * (its host views hold uint8 E4M3 bits); dkv_prefill, dkv_decode_staged and
+ * dkv_attend_naive return UNSUPPORTED for it.  Errors: as the three
+ * allocators, plus INVALID_ARG for an unknown format, UNSUPPORTED for E4M3
+ * with fp16 activations or a paged cache of several layers. */
+dkv_status dkv_cache_alloc_ex(dkv_cache** out, const dkv_cache_desc_t* desc);
 
 /* A layered cache: one pinned allocation each for K and V holding `layers`
  * caches of [batch][n_kv_heads][max_tokens][head_dim] back to back, the

@@ -93,12 +93,18 @@ class Case:
     """A workload materialised on the GPU and in the host cache."""
 
     def __init__(self, w: wl.Workload, lens=None, s_max=None, tuning=None, page_tokens=0,
-                 spare_pages=3, table_seed=0):
+                 spare_pages=3, table_seed=0, kv_format="native"):
         """page_tokens > 0 builds a paged cache: the logical rows of every
         sequence go to pool pages drawn by a seeded permutation (spare pages
-        stay in no table and hold the 0x5A5A canary)."""
+        stay in no table and hold the spare canary).  kv_format "e4m3": the
+        prefix rows are the workload's values rounded to E4M3 (uint8 bits)."""
         import zero_copy_offloaded_gb300 as dkv
         self.w = w
+        self.kv_format = kv_format
+        fp8 = kv_format == "e4m3"
+        self.canary = 0x5A if fp8 else 0x7E57       # rows past the append
+        self.spare_canary = 0x33 if fp8 else 0x5A5A  # pool pages in no table
+        el = np.uint8 if fp8 else np.uint16
         self.dense = wl.make_dense(w)
         self.s_max = s_max or w.S_max
         self.lens = np.broadcast_to(np.asarray(w.P if lens is None else lens, np.int64),
@@ -110,27 +116,32 @@ class Case:
             perm = np.random.default_rng(table_seed).permutation(w.B * npg + spare_pages)
             self.table = perm[:w.B * npg].reshape(w.B, npg).astype(np.int32)
             self.spare = perm[w.B * npg:]
-            self.cache = dkv.PagedKVCache(w.B, w.Hkv, w.D, page_tokens, len(perm), npg, w.dtype)
-            self.cache.k_host[...] = 0x5A5A
-            self.cache.v_host[...] = 0x5A5A
+            self.cache = dkv.PagedKVCache(w.B, w.Hkv, w.D, page_tokens, len(perm), npg, w.dtype,
+                                          kv_format)
+            self.cache.k_host[...] = self.spare_canary
+            self.cache.v_host[...] = self.spare_canary
             self.cache.set_page_table(self.table)
         else:
-            self.cache = dkv.KVCache(w.B, w.Hkv, w.D, self.s_max, w.dtype)
+            self.cache = dkv.KVCache(w.B, w.Hkv, w.D, self.s_max, w.dtype, kv_format)
         # prefix rows: the workload's generator, truncated per sequence
-        kc = np.zeros((w.B, w.Hkv, self.s_max, w.D), np.uint16)
+        kc = np.zeros((w.B, w.Hkv, self.s_max, w.D), el)
         vc = np.zeros_like(kc)
         wp = w.with_(P=int(self.lens.max()))
         for b in range(w.B):
             for h in range(w.Hkv):
                 kk, vv = wl.cache_slice(wp, b, h)
+                if fp8:
+                    import oracle
+                    kk = oracle.round_e4m3(wl.bits_to_f32(kk, w.dtype).astype(np.float64))
+                    vv = oracle.round_e4m3(wl.bits_to_f32(vv, w.dtype).astype(np.float64))
                 n = int(self.lens[b])
                 kc[b, h, :n] = kk[:n]
                 vc[b, h, :n] = vv[:n]
         # canary pattern beyond the prefix: must be overwritten only by appends
         kc[:, :, :, :][np.broadcast_to(np.arange(self.s_max)[None, None, :, None]
-                                       >= self.lens[:, None, None, None], kc.shape)] = 0x7E57
+                                       >= self.lens[:, None, None, None], kc.shape)] = self.canary
         vc[np.broadcast_to(np.arange(self.s_max)[None, None, :, None]
-                           >= self.lens[:, None, None, None], vc.shape)] = 0x7E57
+                           >= self.lens[:, None, None, None], vc.shape)] = self.canary
         if page_tokens:
             self._scatter(self.cache.k_host, kc)
             self._scatter(self.cache.v_host, vc)
@@ -154,7 +165,7 @@ class Case:
 
     def _gather(self, pool):
         pt = self.page_tokens
-        out = np.empty((self.w.B, self.w.Hkv, self.s_max, self.w.D), np.uint16)
+        out = np.empty((self.w.B, self.w.Hkv, self.s_max, self.w.D), pool.dtype)
         for b in range(self.w.B):
             for i, pg in enumerate(self.table[b]):
                 out[b, :, i * pt:(i + 1) * pt] = pool[pg]
@@ -170,8 +181,8 @@ class Case:
     def spare_pages_untouched(self):
         if not self.page_tokens:
             return True
-        return bool(np.all(self.cache.k_host[self.spare] == 0x5A5A) and
-                    np.all(self.cache.v_host[self.spare] == 0x5A5A))
+        return bool(np.all(self.cache.k_host[self.spare] == self.spare_canary) and
+                    np.all(self.cache.v_host[self.spare] == self.spare_canary))
 
     def out_tensor(self, T):
         import torch
@@ -199,7 +210,8 @@ class Case:
         return oracle.step(self.dense["x"] if x_bits is None else x_bits, self.dense["wq"],
                            self.dense["wk"], self.dense["wv"], self.k0 if k is None else k,
                            self.v0 if v is None else v, self.lens if lens is None else lens,
-                           w.Hq, w.dtype, rows=rows)
+                           w.Hq, w.dtype, rows=rows,
+                           kv_format="e4m3" if self.kv_format == "e4m3" else None)
 
     def free(self):
         self.cache.free()

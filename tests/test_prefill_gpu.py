@@ -39,7 +39,7 @@ def check_prefill(case: Case, out, ref, label="", rows=None, beyond_rounding=Fal
             assert_projection_close(got, x[b], wmat, w.dtype, f"{label} {name} append b={b}")
         assert np.array_equal(kh[b, :, :p], case.k0[b, :, :p])
         assert np.array_equal(vh[b, :, :p], case.v0[b, :, :p])
-        assert np.all(kh[b, :, p + T:] == 0x7E57) and np.all(vh[b, :, p + T:] == 0x7E57)
+        assert np.all(kh[b, :, p + T:] == case.canary) and np.all(vh[b, :, p + T:] == case.canary)
     return res
 
 

@@ -26,6 +26,7 @@ __all__ = [
     "dkv_cache_last_kernel_ms", "dkv_cache_alloc_paged", "dkv_cache_set_page_table",
     "PagedKVCache", "LayeredKVCache", "dkv_cache_alloc_layered", "dkv_decode_layer",
     "dkv_prefill_layer", "dkv_step_graph_capture", "dkv_step_graph_launch",
+    "dkv_cache_alloc_ex", "KV_FORMATS",
 ]
 
 BF16 = 0
@@ -57,7 +58,18 @@ class _CacheInfo(ctypes.Structure):
                 ("head_dim", ctypes.c_int), ("max_tokens", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("page_tokens", ctypes.c_int),
                 ("num_pages", ctypes.c_int), ("max_pages_per_seq", ctypes.c_int),
-                ("layers", ctypes.c_int)]
+                ("layers", ctypes.c_int), ("kv_format", ctypes.c_int)]
+
+
+class _CacheDesc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("max_tokens", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("kv_format", ctypes.c_int), ("layers", ctypes.c_int),
+                ("page_tokens", ctypes.c_int), ("num_pages", ctypes.c_int),
+                ("max_pages_per_seq", ctypes.c_int)]
+
+
+KV_FORMATS = {"native": 0, "e4m3": 1}
 
 
 _lib = None
@@ -82,6 +94,7 @@ def lib(build_if_missing: bool = False):
         "dkv_cache_alloc_paged": [ctypes.POINTER(P), I, I, I, I, I, I, I],
         "dkv_cache_set_page_table": [P, P],
         "dkv_cache_alloc_layered": [ctypes.POINTER(P), I, I, I, I, I, I],
+        "dkv_cache_alloc_ex": [ctypes.POINTER(P), ctypes.POINTER(_CacheDesc)],
         "dkv_decode_layer": [P, I, P, P, P, P, I, I, P, P],
         "dkv_prefill_layer": [P, I, P, I, P, P, P, I, I, P, P],
         "dkv_step_graph_capture": [P, I, I, P, P, P, P, P],
@@ -179,6 +192,16 @@ def dkv_cache_set_page_table(h, table):
     """table: int32 [batch, max_pages_per_seq] of pool page indices (-1: none)."""
     t = np.ascontiguousarray(table, dtype=np.int32)
     _check(lib().dkv_cache_set_page_table(h, t.ctypes.data), "dkv_cache_set_page_table")
+
+
+def dkv_cache_alloc_ex(batch, n_kv_heads, head_dim, max_tokens=0, dtype="bf16",
+                       kv_format="native", layers=1, page_tokens=0, num_pages=0,
+                       max_pages_per_seq=0) -> int:
+    d = _CacheDesc(batch, n_kv_heads, head_dim, max_tokens, _DTYPE[dtype], KV_FORMATS[kv_format],
+                   layers, page_tokens, num_pages, max_pages_per_seq)
+    h = ctypes.c_void_p()
+    _check(lib().dkv_cache_alloc_ex(ctypes.byref(h), ctypes.byref(d)), "dkv_cache_alloc_ex")
+    return h.value
 
 
 def dkv_cache_alloc_layered(layers, batch, n_kv_heads, head_dim, max_tokens, dtype="bf16") -> int:
@@ -327,15 +350,19 @@ def dkv_decode_noalloc(x, wq, wk, wv, k_cache, v_cache, lengths, batch, hidden, 
 class KVCache:
     """Owner of one dkv_cache handle, with numpy views of the pinned caches."""
 
-    def __init__(self, batch, n_kv_heads, head_dim, max_tokens, dtype="bf16"):
+    def __init__(self, batch, n_kv_heads, head_dim, max_tokens, dtype="bf16", kv_format="native"):
+        """kv_format "e4m3": 8-bit E4M3 elements (views of uint8 bits; decode only)."""
         self.B, self.Hkv, self.D, self.S_max = batch, n_kv_heads, head_dim, max_tokens
-        self.dtype = dtype
-        self.h = dkv_cache_alloc(batch, n_kv_heads, head_dim, max_tokens, dtype)
+        self.dtype, self.kv_format = dtype, kv_format
+        self.h = dkv_cache_alloc_ex(batch, n_kv_heads, head_dim, max_tokens, dtype, kv_format)
+        self._views((batch, n_kv_heads, max_tokens, head_dim))
+
+    def _views(self, shape):
         kp, vp = dkv_cache_host_ptrs(self.h)
-        shape = (batch, n_kv_heads, max_tokens, head_dim)
         n = int(np.prod(shape))
-        self.k_host = np.ctypeslib.as_array((ctypes.c_uint16 * n).from_address(kp)).reshape(shape)
-        self.v_host = np.ctypeslib.as_array((ctypes.c_uint16 * n).from_address(vp)).reshape(shape)
+        el = ctypes.c_uint8 if self.kv_format == "e4m3" else ctypes.c_uint16
+        self.k_host = np.ctypeslib.as_array((el * n).from_address(kp)).reshape(shape)
+        self.v_host = np.ctypeslib.as_array((el * n).from_address(vp)).reshape(shape)
 
     def set_lengths(self, lens):
         dkv_cache_set_lengths(self.h, np.broadcast_to(np.asarray(lens, np.int32), (self.B,)))
@@ -370,18 +397,14 @@ class PagedKVCache(KVCache):
     ([num_pages, Hkv, page_tokens, D] uint16 each) and the page table."""
 
     def __init__(self, batch, n_kv_heads, head_dim, page_tokens, num_pages, max_pages_per_seq,
-                 dtype="bf16"):
+                 dtype="bf16", kv_format="native"):
         self.B, self.Hkv, self.D = batch, n_kv_heads, head_dim
         self.page_tokens, self.num_pages, self.max_pages = page_tokens, num_pages, max_pages_per_seq
         self.S_max = page_tokens * max_pages_per_seq
-        self.dtype = dtype
-        self.h = dkv_cache_alloc_paged(batch, n_kv_heads, head_dim, page_tokens, num_pages,
-                                       max_pages_per_seq, dtype)
-        kp, vp = dkv_cache_host_ptrs(self.h)
-        shape = (num_pages, n_kv_heads, page_tokens, head_dim)
-        n = int(np.prod(shape))
-        self.k_host = np.ctypeslib.as_array((ctypes.c_uint16 * n).from_address(kp)).reshape(shape)
-        self.v_host = np.ctypeslib.as_array((ctypes.c_uint16 * n).from_address(vp)).reshape(shape)
+        self.dtype, self.kv_format = dtype, kv_format
+        self.h = dkv_cache_alloc_ex(batch, n_kv_heads, head_dim, 0, dtype, kv_format, 1,
+                                    page_tokens, num_pages, max_pages_per_seq)
+        self._views((num_pages, n_kv_heads, page_tokens, head_dim))
         self.table = np.full((batch, max_pages_per_seq), -1, np.int32)
 
     def set_page_table(self, table):
@@ -393,15 +416,13 @@ class LayeredKVCache(KVCache):
     """A whole model's caches: numpy views [layers, B, Hkv, S_max, D] (uint16)
     of the pinned K and V, per-layer decode / prefill and the captured step."""
 
-    def __init__(self, layers, batch, n_kv_heads, head_dim, max_tokens, dtype="bf16"):
+    def __init__(self, layers, batch, n_kv_heads, head_dim, max_tokens, dtype="bf16",
+                 kv_format="native"):
         self.L, self.B, self.Hkv, self.D, self.S_max = layers, batch, n_kv_heads, head_dim, max_tokens
-        self.dtype = dtype
-        self.h = dkv_cache_alloc_layered(layers, batch, n_kv_heads, head_dim, max_tokens, dtype)
-        kp, vp = dkv_cache_host_ptrs(self.h)
-        shape = (layers, batch, n_kv_heads, max_tokens, head_dim)
-        n = int(np.prod(shape))
-        self.k_host = np.ctypeslib.as_array((ctypes.c_uint16 * n).from_address(kp)).reshape(shape)
-        self.v_host = np.ctypeslib.as_array((ctypes.c_uint16 * n).from_address(vp)).reshape(shape)
+        self.dtype, self.kv_format = dtype, kv_format
+        self.h = dkv_cache_alloc_ex(batch, n_kv_heads, head_dim, max_tokens, dtype, kv_format,
+                                    layers)
+        self._views((layers, batch, n_kv_heads, max_tokens, head_dim))
 
     def decode_layer(self, layer, x, wq, wk, wv, n_q_heads, out, stream=None):
         dkv_decode_layer(self.h, layer, x, wq, wk, wv, x.shape[-1], n_q_heads, out, stream)

@@ -27,8 +27,46 @@
 // host cache, the freshly appended one included.
 #include "dkv_internal.cuh"
 
+#include <cuda_fp8.h>
+
 namespace dkv {
 namespace {
+
+// Cache element C: the activation type T itself (2 bytes), or 8-bit E4M3
+// (unscaled, saturating).  pair() turns two adjacent elements, packed in the
+// low bytes of a word, into floats (element at the lower address in .x).
+template <typename T, typename C>
+struct KVE {
+  static constexpr int EB = 2;
+  __device__ static inline float2 pair(uint32_t two) { return DT<T>::to_f2(two); }
+};
+template <typename T>
+struct KVE<T, __nv_fp8_e4m3> {
+  static constexpr int EB = 1;
+  __device__ static inline float2 pair(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
+  }
+};
+
+// The two fp32 sums of a column pair stored as cache elements (rounded once).
+template <typename T, typename C>
+__device__ __forceinline__ void store_pair(C* dst, float a, float b) {
+  if constexpr (KVE<T, C>::EB == 1) {
+    *reinterpret_cast<__nv_fp8x2_storage_t*>(dst) =
+        __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  } else {
+    dst[0] = DT<T>::from_f(a);
+    dst[1] = DT<T>::from_f(b);
+  }
+}
+
+// 16-byte chunk c of cache row n at chunk c ^ (n mod m), m = min(chunks per
+// row, 8): rows read at the same column hit different bank groups.
+template <int CPR>
+__device__ __forceinline__ int swzc(int n, int c) {
+  return c ^ (n & ((CPR < 8 ? CPR : 8) - 1));
+}
 
 // Cached rows of sequence b before this call's append.
 __device__ __forceinline__ int seq_len(const DecodeParams& p, int b) {
@@ -56,13 +94,14 @@ constexpr int kSmemCap = 232448 - 1024;  // dynamic shared memory per CTA, with 
 // at a time, so deeper staging keeps more HBM loads in flight.
 struct DecodeSmem {
   int ring, bars, q, s, alpha, ml, red, wproj, xproj, flag, total, proj_stages;
-  __host__ __device__ DecodeSmem(int D, int G, int N, int stages, int B) {
+  int eb;  // bytes per cache element
+  __host__ __device__ DecodeSmem(int D, int G, int N, int stages, int B, int eb_ = 2) : eb(eb_) {
     for (proj_stages = 4; proj_stages > 2; --proj_stages)
       if (layout(D, G, N, stages, B) <= kSmemCap) break;
     layout(D, G, N, stages, B);
   }
   __host__ __device__ int layout(int D, int G, int N, int stages, int B) {
-    int tile_bytes = N * D * 2;
+    int tile_bytes = N * D * eb;
     int off = 0;
     ring = off; off += stages * 2 * tile_bytes;
     bars = off; off += 2 * stages * 8;
@@ -101,7 +140,7 @@ __device__ __forceinline__ const T* col_source(const DecodeParams& p, int col, i
 // Each output is one fp32 FMA chain over j = 0..H-1 in order (each product of
 // two 16-bit floats is exact in fp32, so the chain equals summing the exact
 // products with one fp32 rounding per step), rounded once to T.
-template <typename T, int D>
+template <typename T, typename C, int D>
 __device__ void project_columns(const DecodeParams& p, int c_begin, int c_end, uint8_t* smem,
                                 const DecodeSmem& L, int ctid) {
   T* wbuf = reinterpret_cast<T*>(smem + L.wproj);   // [S][kProjRows][kProjCols]
@@ -198,17 +237,17 @@ __device__ void project_columns(const DecodeParams& p, int c_begin, int c_end, u
         for (int bb = 0; bb < 2; ++bb) {
           const int b = b0 + bb;
           if (b >= B) break;
-          T v0 = DT<T>::from_f(acc[bb * 2]), v1 = DT<T>::from_f(acc[bb * 2 + 1]);
           if (which == 0) {
             T* q = static_cast<T*>(p.q_ws) + (size_t)b * p.Hq * D + local;
-            q[0] = v0; q[1] = v1;
+            q[0] = DT<T>::from_f(acc[bb * 2]);
+            q[1] = DT<T>::from_f(acc[bb * 2 + 1]);
           } else {
             const int kvh = local / D, d = local % D;
-            T* ws = static_cast<T*>(p.kv_ws) + ((size_t)b * 2 + (which - 1)) * p.Hkv * D + local;
-            ws[0] = v0; ws[1] = v1;
-            T* host = static_cast<T*>(which == 1 ? p.k_host : p.v_host) +
+            C* ws = static_cast<C*>(p.kv_ws) + ((size_t)b * 2 + (which - 1)) * p.Hkv * D + local;
+            store_pair<T, C>(ws, acc[bb * 2], acc[bb * 2 + 1]);
+            C* host = static_cast<C*>(which == 1 ? p.k_host : p.v_host) +
                       p.lay.row(b, kvh, seq_len(p, b), D) + d;
-            host[0] = v0; host[1] = v1;   // the append: one write across the link
+            store_pair<T, C>(host, acc[bb * 2], acc[bb * 2 + 1]);  // the append, across the link
           }
         }
       }
@@ -233,13 +272,16 @@ __device__ __forceinline__ UnitRange unit_range(const DecodeParams& p, int u) {
   return r;
 }
 
-template <typename T, int D, int G>
+template <typename T, typename C, int D, int G>
 __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int EB = KVE<T, C>::EB;
+  constexpr int RB = D * EB;   // bytes per cache row
+  constexpr int EPC = 16 / EB; // elements per 16-byte chunk
   const int N = p.tile_n, stages = p.stages;
-  const DecodeSmem L(D, G, N, stages, p.B);
+  const DecodeSmem L(D, G, N, stages, p.B, EB);
   const int tid = threadIdx.x;
-  const int tile_bytes = N * D * 2;
+  const int tile_bytes = N * RB;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + stages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flag);
@@ -254,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
   __syncthreads();
 
   const int nunits = p.B * p.Hkv * p.splits;
-  constexpr int CPR = D * 2 / 16;  // 16-byte chunks per row
+  constexpr int CPR = RB / 16;  // 16-byte chunks per row
 
   if (tid >= kConsumers) {
     // ------------------------------------------------------------ producer
@@ -263,8 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
     int it = 0;
     for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
       const UnitRange r = unit_range(p, u);
-      const T* kg = static_cast<const T*>(p.k_read);
-      const T* vg = static_cast<const T*>(p.v_read);
+      const C* kg = static_cast<const C*>(p.k_read);
+      const C* vg = static_cast<const C*>(p.v_read);
       // rows read from the host: the cached ones (the fused path takes the new
       // row from HBM), or every row when the projection ran as its own launch
       const int cached = seq_len(p, r.b) + (p.mode == kDecodeAttendOnly ? 1 : 0);
@@ -283,8 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
         const int nrows = max(0, min(N, cached - key0));
         for (int i = ptid; i < nrows * CPR; i += kProducers) {
           const int row = i / CPR, c = i % CPR;
-          const int dst = row * (D * 2) + swz_chunk(row, c) * 16;
-          const size_t src = p.lay.row(r.b, r.kvh, key0 + row, D) + c * 8;
+          const int dst = row * RB + swzc<CPR>(row, c) * 16;
+          const size_t src = p.lay.row(r.b, r.kvh, key0 + row, D) + c * EPC;
           cp_async16(kt + dst, kg + src, 16);
           cp_async16(vt + dst, vg + src, 16);
         }
@@ -308,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
     const int per = nblk / gridDim.x, rem = nblk % gridDim.x;
     const int b0 = blockIdx.x * per + min((int)blockIdx.x, rem);
     const int b1 = b0 + per + ((int)blockIdx.x < rem ? 1 : 0);
-    if (b1 > b0) project_columns<T, D>(p, b0 * 8, b1 * 8, smem, L, ctid);
+    if (b1 > b0) project_columns<T, C, D>(p, b0 * 8, b1 * 8, smem, L, ctid);
   }
   if (p.mode == kDecodeProjectOnly) return;  // the producers returned at once
   if (p.mode == kDecodeFused) {
@@ -381,9 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
       const int rnew = seq_len(p, r.b) - key0;
       if (p.mode == kDecodeFused && rnew >= 0 && rnew < N && ctid < 2 * CPR) {
         const int which = ctid / CPR, c = ctid % CPR;
-        const T* src = static_cast<const T*>(p.kv_ws) +
-                       ((size_t)r.b * 2 + which) * p.Hkv * D + r.kvh * D + c * 8;
-        uint8_t* dst = (which ? vt : kt) + rnew * (D * 2) + swz_chunk(rnew, c) * 16;
+        const C* src = static_cast<const C*>(p.kv_ws) +
+                       ((size_t)r.b * 2 + which) * p.Hkv * D + r.kvh * D + c * EPC;
+        uint8_t* dst = (which ? vt : kt) + rnew * RB + swzc<CPR>(rnew, c) * 16;
         *reinterpret_cast<uint4*>(dst) = __ldcg(reinterpret_cast<const uint4*>(src));
       }
       named_bar_sync(kBarConsumers, kConsumers);
@@ -398,19 +440,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
         float dot = 0.f;
         if (n < nvalid) {
           const float* qrow = q_s + g * (D + 4) + part * DPT;
-          const uint8_t* krow = kt + n * (D * 2);
+          const uint8_t* krow = kt + n * RB;
 #pragma unroll 4
-          for (int c8 = 0; c8 < DPT / 8; ++c8) {
-            const int c = part * (DPT / 8) + c8;
-            const uint4 kv = *reinterpret_cast<const uint4*>(krow + swz_chunk(n, c) * 16);
-            const float4 qa = *reinterpret_cast<const float4*>(qrow + c8 * 8);
-            const float4 qb = *reinterpret_cast<const float4*>(qrow + c8 * 8 + 4);
-            float2 k0 = DT<T>::to_f2(kv.x), k1 = DT<T>::to_f2(kv.y);
-            float2 k2 = DT<T>::to_f2(kv.z), k3 = DT<T>::to_f2(kv.w);
-            dot = fmaf(qa.x, k0.x, dot); dot = fmaf(qa.y, k0.y, dot);
-            dot = fmaf(qa.z, k1.x, dot); dot = fmaf(qa.w, k1.y, dot);
-            dot = fmaf(qb.x, k2.x, dot); dot = fmaf(qb.y, k2.y, dot);
-            dot = fmaf(qb.z, k3.x, dot); dot = fmaf(qb.w, k3.y, dot);
+          for (int c8 = 0; c8 < DPT / EPC; ++c8) {
+            const int c = part * (DPT / EPC) + c8;
+            const uint4 kv = *reinterpret_cast<const uint4*>(krow + swzc<CPR>(n, c) * 16);
+            const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+            for (int e = 0; e < EPC / 2; ++e) {
+              // pair e of the chunk: word e (16-bit elements) or half-word e (8-bit)
+              const uint32_t two = EB == 2 ? w4[e] : (w4[e / 2] >> (16 * (e % 2)));
+              const float2 k = KVE<T, C>::pair(two);
+              const float2 q = *reinterpret_cast<const float2*>(qrow + c8 * EPC + 2 * e);
+              dot = fmaf(q.x, k.x, dot);
+              dot = fmaf(q.y, k.y, dot);
+            }
           }
         }
         for (int off = TPS / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
@@ -452,12 +496,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
         const float a = alpha_s[buf * G + g];
         float o0 = acc[pp][0] * a, o1 = acc[pp][1] * a;
         const float* prow = sb + g * N;
-        const int c = dp / 4, within = (dp % 4) * 4;
+        const int c = dp / (EPC / 2), within = (dp % (EPC / 2)) * 2 * EB;
         for (int n = kgi; n < nvalid; n += KG) {
           const float pw = prow[n];
-          const uint32_t v2 = *reinterpret_cast<const uint32_t*>(vt + n * (D * 2) +
-                                                                swz_chunk(n, c) * 16 + within);
-          const float2 v = DT<T>::to_f2(v2);
+          const uint8_t* vp = vt + n * RB + swzc<CPR>(n, c) * 16 + within;
+          const uint32_t v2 = EB == 2 ? *reinterpret_cast<const uint32_t*>(vp)
+                                      : (uint32_t)*reinterpret_cast<const uint16_t*>(vp);
+          const float2 v = KVE<T, C>::pair(v2);
           o0 = fmaf(pw, v.x, o0);
           o1 = fmaf(pw, v.y, o1);
         }
@@ -520,10 +565,10 @@ __global__ void decode_combine_kernel(const float* __restrict__ part_o,
   if (blockIdx.x == 0 && threadIdx.x == 0) status->grid_arrive = 0u;
 }
 
-template <typename T, int D, int G>
+template <typename T, typename C, int D, int G>
 cudaError_t launch_decode_t(const DecodeParams& p, int grid, int smem, cudaStream_t s,
                             const KernelTimer& timer) {
-  auto kern = decode_fused_kernel<T, D, G>;
+  auto kern = decode_fused_kernel<T, C, D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   timer.before(s);
@@ -554,20 +599,28 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, int smem, cudaStrea
   return cudaGetLastError();
 }
 
-template <typename T, int D, int G>
+template <typename T, typename C, int D, int G>
 cudaError_t occupancy_t(int smem, int* blocks) {
-  auto kern = decode_fused_kernel<T, D, G>;
+  auto kern = decode_fused_kernel<T, C, D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, kern, kThreads, smem);
 }
 
-// Kernel repository: <dtype, head_dim, group size> instantiations.
+// Kernel repository: <activation type, cache element, head_dim, group size>
+// instantiations; `dtype` is the activation dtype, kv_fp8 selects E4M3 caches
+// (bf16 activations only).
 template <typename F>
-cudaError_t dispatch(int dtype, int D, int G, F&& f) {
+cudaError_t dispatch(int dtype, bool kv_fp8, int D, int G, F&& f) {
 #define DKV_CASE(TT, DD, GG) \
-  if (D == DD && G == GG) return f.template operator()<TT, DD, GG>();
-  if (dtype == DKV_BF16) {
+  if (D == DD && G == GG) return f.template operator()<TT, TT, DD, GG>();
+#define DKV_CASE8(DD, GG) \
+  if (D == DD && G == GG) return f.template operator()<__nv_bfloat16, __nv_fp8_e4m3, DD, GG>();
+  if (kv_fp8) {
+    if (dtype != DKV_BF16) return cudaErrorInvalidValue;
+    DKV_CASE8(64, 1) DKV_CASE8(64, 2) DKV_CASE8(64, 4) DKV_CASE8(64, 8)
+    DKV_CASE8(128, 1) DKV_CASE8(128, 2) DKV_CASE8(128, 4) DKV_CASE8(128, 8)
+  } else if (dtype == DKV_BF16) {
     DKV_CASE(__nv_bfloat16, 64, 1) DKV_CASE(__nv_bfloat16, 64, 2) DKV_CASE(__nv_bfloat16, 64, 4)
     DKV_CASE(__nv_bfloat16, 64, 8) DKV_CASE(__nv_bfloat16, 128, 1) DKV_CASE(__nv_bfloat16, 128, 2)
     DKV_CASE(__nv_bfloat16, 128, 4) DKV_CASE(__nv_bfloat16, 128, 8)
@@ -577,6 +630,7 @@ cudaError_t dispatch(int dtype, int D, int G, F&& f) {
     DKV_CASE(__half, 128, 4) DKV_CASE(__half, 128, 8)
   }
 #undef DKV_CASE
+#undef DKV_CASE8
   return cudaErrorInvalidValue;
 }
 
@@ -592,36 +646,36 @@ cudaError_t launch_advance_lengths(int* len, int B, int T, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-int decode_smem_bytes(int dtype, int D, int G, int tile_n, int stages, int B) {
+int decode_smem_bytes(int dtype, int D, int G, int tile_n, int stages, int B, bool kv_fp8) {
   (void)dtype;
-  return DecodeSmem(D, G, tile_n, stages, B).total;
+  return DecodeSmem(D, G, tile_n, stages, B, kv_fp8 ? 1 : 2).total;
 }
 
 struct LaunchDecodeF {
   const DecodeParams* p; int grid; int smem; cudaStream_t s; const KernelTimer* timer;
-  template <typename T, int D, int G> cudaError_t operator()() {
-    return launch_decode_t<T, D, G>(*p, grid, smem, s, *timer);
+  template <typename T, typename C, int D, int G> cudaError_t operator()() {
+    return launch_decode_t<T, C, D, G>(*p, grid, smem, s, *timer);
   }
 };
 struct OccF {
   int smem; int* blocks;
-  template <typename T, int D, int G> cudaError_t operator()() {
-    return occupancy_t<T, D, G>(smem, blocks);
+  template <typename T, typename C, int D, int G> cudaError_t operator()() {
+    return occupancy_t<T, C, D, G>(smem, blocks);
   }
 };
 
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int grid, int smem_bytes,
                           cudaStream_t s, int* launches, const KernelTimer& timer) {
   LaunchDecodeF f{&p, grid, smem_bytes, s, &timer};
-  cudaError_t e = dispatch(dtype, p.D, p.Hq / p.Hkv, f);
+  cudaError_t e = dispatch(dtype, p.kv_fp8 != 0, p.D, p.Hq / p.Hkv, f);
   if (e == cudaSuccess && launches) *launches += p.mode == kDecodeProjectOnly ? 1 : 2;
   return e;
 }
 
 cudaError_t decode_occupancy(int dtype, int D, int G, int tile_n, int stages, int B,
-                             int* blocks_per_sm) {
-  OccF f{decode_smem_bytes(dtype, D, G, tile_n, stages, B), blocks_per_sm};
-  return dispatch(dtype, D, G, f);
+                             int* blocks_per_sm, bool kv_fp8) {
+  OccF f{decode_smem_bytes(dtype, D, G, tile_n, stages, B, kv_fp8), blocks_per_sm};
+  return dispatch(dtype, kv_fp8, D, G, f);
 }
 
 }  // namespace dkv

@@ -84,6 +84,8 @@ struct dkv_cache {
   int page_tokens, page_shift, num_pages, max_pages;
   std::vector<int32_t> pages;  // host copy of the page table [B][max_pages], -1 = none
   int* pages_dev;              // device copy read by the kernels
+  // cache element format: DKV_KV_NATIVE (the dtype, 2 bytes) or DKV_KV_E4M3
+  int kv_format, kv_eb;
   // layered caches: `layers` caches of layer_elems elements each for K and V
   int layers;
   size_t layer_elems;
@@ -126,8 +128,8 @@ dkv_status ensure_ws(dkv_cache* c, size_t need) {
 constexpr double kAlpha = 0.8;          // share of the L1/shared pool used as SMEM
 constexpr double kPoolBytes = 256 * 1024;  // unified L1/shared pool per SM
 
-bool smem_constraint_ok(int D, int N, int m) {
-  return kAlpha * kPoolBytes >= 3.0 * m * 2.0 * (double)D * N;
+bool smem_constraint_ok(int D, int N, int m, int eb) {
+  return kAlpha * kPoolBytes >= 3.0 * m * (double)eb * D * N;
 }
 
 struct DecodeChoice {
@@ -136,16 +138,20 @@ struct DecodeChoice {
 
 dkv_status choose_decode(dkv_cache* c, int G, DecodeChoice* ch) {
   const int D = c->D;
-  int N = c->tune_tile > 0 ? c->tune_tile : 8192 / D;  // one 16 KB K tile + one 16 KB V tile
+  const bool fp8 = c->kv_format == DKV_KV_E4M3;
+  // one 16 KB K tile + one 16 KB V tile
+  int N = c->tune_tile > 0 ? c->tune_tile : 16384 / (D * c->kv_eb);
   int m = c->tune_stages > 0 ? c->tune_stages : 4;
   if ((N != 32 && N != 64 && N != 128 && N != 256) || m < 2 || m > 8)
     return fail(DKV_ERR_INVALID_ARG, "tuning tile_n=%d stages=%d out of range", N, m);
-  while (m > 2 && !smem_constraint_ok(D, N, m)) --m;
-  if (!smem_constraint_ok(D, N, m))
+  while (m > 2 && !smem_constraint_ok(D, N, m, c->kv_eb)) --m;
+  if (!smem_constraint_ok(D, N, m, c->kv_eb))
     return fail(DKV_ERR_UNSUPPORTED, "tile %d x %d fails the shared-memory constraint", N, D);
-  const int smem = decode_smem_bytes(c->dtype, D, G, N, m, c->B);
+  if (fp8 && N * G < 256 && (D / (256 / (N * G))) % 16 != 0)
+    return fail(DKV_ERR_UNSUPPORTED, "tile %d: an E4M3 score slice must span whole 16-byte chunks", N);
+  const int smem = decode_smem_bytes(c->dtype, D, G, N, m, c->B, fp8);
   int occ = 0;
-  cudaError_t e = decode_occupancy(c->dtype, D, G, N, m, c->B, &occ);
+  cudaError_t e = decode_occupancy(c->dtype, D, G, N, m, c->B, &occ, fp8);
   if (e != cudaSuccess) return cuda_fail(e, "decode occupancy");
   if (occ < 1) return fail(DKV_ERR_UNSUPPORTED, "decode kernel does not fit on an SM (smem %d)", smem);
   const int grid = c->sms * occ;
@@ -247,7 +253,7 @@ dkv_status decode_impl(dkv_cache* c, const void* x, const void* wq, const void* 
   memset(&p, 0, sizeof p);
   char* w = static_cast<char*>(c->ws.base);
   p.x = x; p.wq = wq; p.wk = wk; p.wv = wv;
-  const size_t loff = (size_t)layer * c->layer_elems * 2;  // bytes
+  const size_t loff = (size_t)layer * c->layer_elems * c->kv_eb;  // bytes
   p.k_read = static_cast<const char*>(k_read) + loff;
   p.v_read = static_cast<const char*>(v_read) + loff;
   p.k_host = static_cast<char*>(c->k_dev) + loff;
@@ -262,6 +268,7 @@ dkv_status decode_impl(dkv_cache* c, const void* x, const void* wq, const void* 
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   p.debug_withhold = c->debug_withhold;
   p.lay = layout_of(c);
+  p.kv_fp8 = c->kv_format == DKV_KV_E4M3;
   fill_lens(p.len, c->len);
   if (capture) p.len_dev = c->len_dev;
   if (!capture) g_last_launches = 0;
@@ -324,7 +331,8 @@ int dkv_last_launch_count(void) { return g_last_launches; }
 // elements each for K and for V in pinned, mapped host memory.
 static dkv_status alloc_common(dkv_cache** out, int batch, int n_kv_heads, int head_dim,
                                int max_tokens, dkv_dtype dtype, size_t rows, int page_tokens,
-                               int num_pages, int max_pages, int layers = 1) {
+                               int num_pages, int max_pages, int layers = 1,
+                               int kv_format = DKV_KV_NATIVE) {
   if (!out) return fail(DKV_ERR_INVALID_ARG, "null output handle");
   *out = nullptr;
   if (batch <= 0 || batch > kMaxBatch)
@@ -348,7 +356,12 @@ static dkv_status alloc_common(dkv_cache** out, int batch, int n_kv_heads, int h
   cudaDeviceGetAttribute(&can_map, cudaDevAttrCanMapHostMemory, dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (!can_map) return fail(DKV_ERR_NO_MAPPED_MEMORY, "device %d cannot map host memory", dev);
-  const size_t bytes = rows * head_dim * 2 * layers;
+  if (kv_format != DKV_KV_NATIVE && kv_format != DKV_KV_E4M3)
+    return fail(DKV_ERR_INVALID_ARG, "kv_format=%d is not native (0) or E4M3 (1)", kv_format);
+  if (kv_format == DKV_KV_E4M3 && dtype != DKV_BF16)
+    return fail(DKV_ERR_UNSUPPORTED, "E4M3 caches take bf16 activations");
+  const int kv_eb = kv_format == DKV_KV_E4M3 ? 1 : 2;
+  const size_t bytes = rows * head_dim * kv_eb * layers;
   void* kh = nullptr;
   void* vh = nullptr;
   e = cudaHostAlloc(&kh, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
@@ -426,6 +439,8 @@ static dkv_status alloc_common(dkv_cache** out, int batch, int n_kv_heads, int h
   c->pages_dev = pages_dev;
   c->layers = layers;
   c->layer_elems = rows * head_dim;
+  c->kv_format = kv_format;
+  c->kv_eb = kv_eb;
   c->len_dev = len_dev;
   c->len_dev_stale = false;
   c->step_exec = nullptr;
@@ -460,6 +475,36 @@ dkv_status dkv_cache_alloc(dkv_cache** out, int batch, int n_kv_heads, int head_
                 n_kv_heads, max_tokens);
   return alloc_common(out, batch, n_kv_heads, head_dim, max_tokens, dtype,
                       (size_t)batch * n_kv_heads * max_tokens, 0, 0, 0);
+}
+
+dkv_status dkv_cache_alloc_ex(dkv_cache** out, const dkv_cache_desc_t* d) {
+  if (!out) return fail(DKV_ERR_INVALID_ARG, "null output handle");
+  *out = nullptr;
+  if (!d) return fail(DKV_ERR_INVALID_ARG, "null description");
+  const int layers = d->layers > 0 ? d->layers : 1;
+  if (layers > 1024) return fail(DKV_ERR_INVALID_ARG, "layers=%d must be in [1, 1024]", layers);
+  if (d->batch <= 0 || d->batch > kMaxBatch)
+    return fail(DKV_ERR_INVALID_ARG, "batch=%d must be in [1, %d]", d->batch, kMaxBatch);
+  if (d->n_kv_heads <= 0)
+    return fail(DKV_ERR_INVALID_ARG, "n_kv_heads=%d must be positive", d->n_kv_heads);
+  if (d->page_tokens) {
+    if (layers != 1) return fail(DKV_ERR_UNSUPPORTED, "paged caches hold one layer");
+    if (d->page_tokens < 1 || d->page_tokens > 4096 || (d->page_tokens & (d->page_tokens - 1)))
+      return fail(DKV_ERR_INVALID_ARG, "page_tokens=%d must be a power of two in [1, 4096]",
+                  d->page_tokens);
+    if (d->num_pages <= 0 || d->max_pages_per_seq <= 0)
+      return fail(DKV_ERR_INVALID_ARG, "num_pages and max_pages_per_seq must be positive");
+    if ((long long)d->max_pages_per_seq * d->page_tokens > (1LL << 30))
+      return fail(DKV_ERR_INVALID_ARG, "max_pages_per_seq * page_tokens is too large");
+    return alloc_common(out, d->batch, d->n_kv_heads, d->head_dim,
+                        d->max_pages_per_seq * d->page_tokens, d->dtype,
+                        (size_t)d->num_pages * d->n_kv_heads * d->page_tokens, d->page_tokens,
+                        d->num_pages, d->max_pages_per_seq, 1, d->kv_format);
+  }
+  if (d->max_tokens <= 0) return fail(DKV_ERR_INVALID_ARG, "max_tokens=%d must be positive", d->max_tokens);
+  return alloc_common(out, d->batch, d->n_kv_heads, d->head_dim, d->max_tokens, d->dtype,
+                      (size_t)d->batch * d->n_kv_heads * d->max_tokens, 0, 0, 0, layers,
+                      d->kv_format);
 }
 
 dkv_status dkv_cache_alloc_paged(dkv_cache** out, int batch, int n_kv_heads, int head_dim,
@@ -566,7 +611,7 @@ dkv_status dkv_cache_get_lengths(const dkv_cache* c, int32_t* len) {
 
 dkv_status dkv_cache_info(const dkv_cache* c, dkv_cache_info_t* info) {
   if (!valid(c) || !info) return fail(DKV_ERR_INVALID_ARG, "invalid argument");
-  info->host_pinned_bytes = 2 * pool_rows(c) * c->D * 2 * c->layers;
+  info->host_pinned_bytes = 2 * pool_rows(c) * c->D * c->kv_eb * c->layers;
   info->device_workspace_bytes = c->ws.bytes + sizeof(DeviceStatus) +
                                  c->pages.size() * sizeof(int32_t);
   info->device_staging_bytes = 0;
@@ -575,6 +620,7 @@ dkv_status dkv_cache_info(const dkv_cache* c, dkv_cache_info_t* info) {
   info->page_tokens = c->page_tokens; info->num_pages = c->num_pages;
   info->max_pages_per_seq = c->max_pages;
   info->layers = c->layers;
+  info->kv_format = c->kv_format;
   return DKV_OK;
 }
 
@@ -738,8 +784,8 @@ dkv_status dkv_decode_staged(dkv_cache* c, const void* x, const void* wq, const 
   dkv_status st = check_call(c, x, wq, wk, wv, hidden, n_q_heads, out, 1);
   if (st != DKV_OK) return st;
   if (!k_stage || !v_stage) return fail(DKV_ERR_INVALID_ARG, "null staging buffer");
-  if (c->page_tokens || c->layers != 1)
-    return fail(DKV_ERR_UNSUPPORTED, "staged decode needs a dense one-layer cache");
+  if (c->page_tokens || c->layers != 1 || c->kv_format != DKV_KV_NATIVE)
+    return fail(DKV_ERR_UNSUPPORTED, "staged decode needs a dense one-layer 16-bit cache");
   std::lock_guard<std::mutex> lk(c->mu);
   if ((st = set_device(c)) != DKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -767,6 +813,8 @@ dkv_status dkv_prefill_layer(dkv_cache* c, int layer, const void* x, int T, cons
   if (st != DKV_OK) return st;
   if (layer < 0 || layer >= c->layers)
     return fail(DKV_ERR_INVALID_ARG, "layer %d outside [0, %d)", layer, c->layers);
+  if (c->kv_format != DKV_KV_NATIVE)
+    return fail(DKV_ERR_UNSUPPORTED, "prefill needs a 16-bit cache (E4M3 caches serve decode)");
   std::lock_guard<std::mutex> lk(c->mu);
   if ((st = set_device(c)) != DKV_OK) return st;
   const int G = n_q_heads / c->Hkv;
@@ -903,8 +951,8 @@ dkv_status dkv_probe_write(void* dst, size_t bytes, void* stream) {
 dkv_status dkv_attend_naive(dkv_cache* c, const void* q, int n_q_heads, void* out, void* stream) {
   if (!valid(c) || !q || !out || n_q_heads <= 0 || n_q_heads % c->Hkv)
     return fail(DKV_ERR_INVALID_ARG, "invalid argument");
-  if (c->page_tokens || c->layers != 1)
-    return fail(DKV_ERR_UNSUPPORTED, "naive attention needs a dense one-layer cache");
+  if (c->page_tokens || c->layers != 1 || c->kv_format != DKV_KV_NATIVE)
+    return fail(DKV_ERR_UNSUPPORTED, "naive attention needs a dense one-layer 16-bit cache");
   std::lock_guard<std::mutex> lk(c->mu);
   dkv_status st = set_device(c);
   if (st != DKV_OK) return st;

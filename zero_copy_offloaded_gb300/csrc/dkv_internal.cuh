@@ -204,6 +204,7 @@ struct DecodeParams {
   int debug_withhold;  // test hook: producers never signal their first tile
   CacheLayout lay;     // rows of k_read / v_read / k_host / v_host
   int mode;            // DecodeMode
+  int kv_fp8;          // caches hold 8-bit E4M3 (bf16 activations)
   // lengths: len_dev (device, [B]) when set, so that a captured graph replays
   // with the lengths of the step it runs; else the by-value copy below
   const int* len_dev;
@@ -245,9 +246,9 @@ cudaError_t launch_decode(const DecodeParams& p, int dtype, int grid, int smem_b
                           cudaStream_t s, int* launches, const KernelTimer& timer);
 // len[b] += T for b < B (the last node of a captured decode step).
 cudaError_t launch_advance_lengths(int* len, int B, int T, cudaStream_t s);
-int decode_smem_bytes(int dtype, int D, int G, int tile_n, int stages, int B);
+int decode_smem_bytes(int dtype, int D, int G, int tile_n, int stages, int B, bool kv_fp8 = false);
 cudaError_t decode_occupancy(int dtype, int D, int G, int tile_n, int stages, int B,
-                             int* blocks_per_sm);
+                             int* blocks_per_sm, bool kv_fp8 = false);
 bool decode_supported(int dtype, int D, int G);
 
 // Tensor-core prefill (prefill_tc.cu): Q projection, fused KV-stationary
