@@ -170,6 +170,31 @@ def test_decode_longctx_spiked():
         case.free()
 
 
+def test_decode_max_batch():
+    """The largest batch a call takes (64 sequences), ragged lengths including 0."""
+    w = wl.Workload("t", "decode", B=64, H=128, Hq=8, Hkv=2, D=64, P=200, seed=64)
+    lens = [(7 * b) % 201 for b in range(64)]
+    case = Case(w, lens=lens, s_max=210)
+    try:
+        out = case.run_decode()
+        check_decode(case, out, case.oracle(), "B=64")
+        assert list(case.cache.lengths()) == [n + 1 for n in lens]
+    finally:
+        case.free()
+
+
+@pytest.mark.slow
+def test_decode_longctx_128k_full():
+    """One sequence at 131072 cached keys (1 % of keys x8), every query head
+    against the full oracle."""
+    case = Case(wl.WORKLOADS["longctx_b1_s128k"])
+    try:
+        out = case.run_decode()
+        check_decode(case, out, case.oracle(), "longctx_b1_s128k")
+    finally:
+        case.free()
+
+
 @pytest.mark.slow
 def test_decode_mha_fp16_full_size():
     case = Case(wl.WORKLOADS["mha_fp16_decode"])

@@ -94,6 +94,19 @@ def test_prefill_spiky_keys(dtype):
         case.free()
 
 
+def test_prefill_max_batch():
+    """64 sequences (the largest batch), ragged prefixes including 0, T crossing a chunk."""
+    w = wl.Workload("t", "prefill", B=64, H=64, Hq=4, Hkv=2, D=64, P=300, T=20, seed=65)
+    lens = [(13 * b) % 301 for b in range(64)]
+    case = Case(w, lens=lens, s_max=330)
+    try:
+        out = case.run_prefill()
+        check_prefill(case, out, case.oracle(), "prefill B=64")
+        assert list(case.cache.lengths()) == [n + 20 for n in lens]
+    finally:
+        case.free()
+
+
 def test_prefill_ragged_lengths():
     w = wl.Workload("t", "prefill", B=3, H=64, Hq=8, Hkv=2, D=128, P=520, T=40, seed=4)
     case = Case(w, lens=[0, 520, 257], s_max=600)
