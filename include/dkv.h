@@ -29,7 +29,10 @@
  *     [B, T, Hq, D]; all row-major, all in the cache's dtype, all DEVICE
  *     pointers owned by the caller.
  *   - The K cache and the V cache are each [B][Hkv][max_tokens][D] in pinned,
- *     mapped host memory owned by the library.
+ *     mapped host memory owned by the library (dense caches; paged caches
+ *     hold pools of pages, layered caches one such pair per layer, see
+ *     their allocators).  Elements are the dtype, or 8-bit E4M3 for caches
+ *     allocated with that format.
  *   - A stream argument is a cudaStream_t passed as void* (NULL = the legacy
  *     default stream).  Work is enqueued; nothing waits for the GPU unless
  *     the call says so.
@@ -50,8 +53,10 @@ extern "C" {
 typedef enum {
     DKV_OK = 0,
     DKV_ERR_INVALID_ARG = 1,      /* null pointer, bad size, bad handle */
-    DKV_ERR_UNSUPPORTED = 2,      /* no precompiled kernel for (dtype, D, G) */
-    DKV_ERR_CAPACITY = 3,         /* length + T would exceed max_tokens */
+    DKV_ERR_UNSUPPORTED = 2,      /* no precompiled kernel for (dtype, D, G), or a
+                                     call that this kind of cache does not serve */
+    DKV_ERR_CAPACITY = 3,         /* length + T would exceed max_tokens, or a row
+                                     of a paged cache has no page */
     DKV_ERR_NO_MAPPED_MEMORY = 4, /* the device cannot map host memory */
     DKV_ERR_ALLOC = 5,            /* pinned host or device allocation failed */
     DKV_ERR_CUDA = 6,             /* a CUDA runtime call failed */
@@ -189,9 +194,11 @@ dkv_status dkv_cache_reserve(dkv_cache* cache, int n_q_heads, int max_new_tokens
  * of the Hq query heads over keys 0..len[b] of their KV head (the new token
  * included), written to out [B, 1, Hq, D].  Lengths advance by 1 when the
  * call is enqueued.  One cooperative launch of the fused kernel plus a
- * split-KV combine launch.  Errors: INVALID_ARG, UNSUPPORTED (dtype, D,
- * Hq/Hkv), CAPACITY, ALLOC (workspace growth), CUDA.  Device-side wait
- * timeouts are reported by dkv_sync_status. */
+ * split-KV combine launch.  With an E4M3 cache the new k, v are the fp32
+ * sums rounded once to E4M3 and the attention reads the decoded E4M3 rows.
+ * Errors: INVALID_ARG (also for a layered cache: use dkv_decode_layer),
+ * UNSUPPORTED (dtype, D, Hq/Hkv), CAPACITY, ALLOC (workspace growth), CUDA.
+ * Device-side wait timeouts are reported by dkv_sync_status. */
 dkv_status dkv_decode(dkv_cache* cache, const void* x, const void* wq, const void* wk,
                       const void* wv, int hidden, int n_q_heads, void* out, void* stream);
 
@@ -232,7 +239,7 @@ dkv_status dkv_step_graph_launch(dkv_cache* cache, void* stream);
  * in place and appending them to the host cache, and runs every query tile
  * of the KV head against it; a combine launch merges the per-chunk partial
  * results.  out is [B, T, Hq, D].  Lengths advance by T when enqueued.
- * Errors as dkv_decode. */
+ * Errors as dkv_decode, plus UNSUPPORTED for an E4M3 cache. */
 dkv_status dkv_prefill(dkv_cache* cache, const void* x, int T, const void* wq, const void* wk,
                        const void* wv, int hidden, int n_q_heads, void* out, void* stream);
 
