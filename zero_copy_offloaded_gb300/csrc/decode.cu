@@ -369,8 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
         }
       }
     }
-    named_bar_sync(kBarConsumers, kConsumers);
-    if (*abort_flag) return;  // producers see the flag in their bounded waits
+    // one decision for all consumers: a producer may raise the flag between
+    // two of them reading it, and a consumer that went on alone would wait at
+    // the next named barrier for warps that had left
+    if (named_bar_sync_or(kBarConsumers, kConsumers, *abort_flag != 0)) return;
   }
 
   float* q_s = reinterpret_cast<float*>(smem + L.q);     // [G][D+4]
@@ -428,8 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
         uint8_t* dst = (which ? vt : kt) + rnew * RB + swzc<CPR>(rnew, c) * 16;
         *reinterpret_cast<uint4*>(dst) = __ldcg(reinterpret_cast<const uint4*>(src));
       }
-      named_bar_sync(kBarConsumers, kConsumers);
-      if (*abort_flag) return;
+      if (named_bar_sync_or(kBarConsumers, kConsumers, *abort_flag != 0)) return;
 
       // scores s[g][n] = (q_g . k_n) * log2(e)/sqrt(D)
       float* sb = s_s + buf * G * N;
