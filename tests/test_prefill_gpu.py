@@ -57,16 +57,29 @@ def test_prefill_shapes(dtype, D, Hq, Hkv, P, T):
         case.free()
 
 
+def _late_max_fraction(ref, K, w, nchunks):
+    """Fraction of (query row, prefix chunk) pairs whose scores past the
+    chunk's first 64 keys exceed the max of those 64 by more than 2^15 in
+    weight: the pairs where the fused kernel rescales the weights it has
+    already written (computed from the oracle's q, in fp64)."""
+    q = wl.bits_to_f32(ref["q"], w.dtype).astype(np.float64)  # [B,T,Hq,D]
+    G = w.Hq // w.Hkv
+    hits = total = 0
+    for b in range(w.B):
+        for h in range(w.Hq):
+            s = q[b, :, h] @ K[b, h // G, :nchunks * 256].T / np.sqrt(w.D) * np.log2(np.e)
+            for c in range(nchunks):  # chunks wholly in the prefix: every query sees them
+                m0 = s[:, c * 256:c * 256 + 64].max(axis=1)
+                m1 = s[:, c * 256 + 64:c * 256 + 256].max(axis=1)
+                hits += int(np.sum(m1 > m0 + 15))
+                total += m0.size
+    return hits / total
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 def test_prefill_spiky_keys(dtype):
-    """5 % of the cached key rows scaled by 8 (the long-context recipe, denser).
-
-    The fused kernel forms a row's weights for the first 128 keys of a chunk
-    against their own max and rescales them only when the second 128 keys'
-    max is larger by more than a factor 2^8 in weight; spikes make that common, so both ways
-    through the softmax are compared with the oracle.  The fraction of (query
-    row, prefix chunk) pairs that take the rescale is computed here from the
-    oracle's q, so the case is known to exercise it."""
+    """5 % of the cached key rows scaled by 8 (the long-context recipe, denser):
+    attention concentrates on few keys, and the outputs on single value rows."""
     w = wl.Workload("t", "prefill", B=2, H=128, Hq=8, Hkv=2, D=128, P=700, T=90, dtype=dtype,
                     kv_dist="uniform2" if dtype == "fp16" else "normal", spike_frac=0.05,
                     seed=11)
@@ -77,19 +90,35 @@ def test_prefill_spiky_keys(dtype):
         # attention concentrates on single value rows, so outputs reach |o| >= 4
         # where bf16's own rounding exceeds the flat max-abs bar
         check_prefill(case, out, ref, f"spiky {dtype}", beyond_rounding=True)
-        q = wl.bits_to_f32(ref["q"], dtype).astype(np.float64)  # [B,T,Hq,D]
-        K = wl.bits_to_f32(case.k0, dtype).astype(np.float64)  # [B,Hkv,s_max,D]
-        G = w.Hq // w.Hkv
-        hits = total = 0
-        for b in range(w.B):
-            for h in range(w.Hq):
-                s = q[b, :, h] @ K[b, h // G, :512].T / np.sqrt(w.D) * np.log2(np.e)
-                for c in range(2):  # chunks wholly in the prefix: every query sees them
-                    m0 = s[:, c * 256:c * 256 + 128].max(axis=1)
-                    m1 = s[:, c * 256 + 128:c * 256 + 256].max(axis=1)
-                    hits += int(np.sum(m1 > m0 + 8))
-                    total += m0.size
-        assert hits / total > 0.05, f"rescale taken by only {hits}/{total} rows"
+    finally:
+        case.free()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_prefill_late_key_spikes(dtype):
+    """The key at offset 200 of every 256-key chunk scaled by 40.
+
+    The fused kernel forms a row's weights against the max of the chunk's
+    first 64 scores and, when a later score exceeds that max by more than
+    2^15 in weight, rescales the weights it has written and continues
+    against the new max.  Here that happens for a known share of the rows
+    (asserted from the oracle's q), and the outputs are compared with the
+    oracle as everywhere else."""
+    w = wl.Workload("t", "prefill", B=2, H=128, Hq=8, Hkv=2, D=128, P=768, T=64, dtype=dtype,
+                    kv_dist="uniform2" if dtype == "fp16" else "normal", seed=23)
+    case = Case(w, s_max=w.P + w.T + 3)
+    try:
+        kf = wl.bits_to_f32(case.k0, dtype)
+        rows = np.arange(200, w.P, 256)
+        kf[:, :, rows] *= np.float32(40.0)
+        case.k0[:, :, rows] = wl.to_bits(kf[:, :, rows], dtype)
+        case.cache.k_host[...] = case.k0
+        out = case.run_prefill()
+        ref = case.oracle()
+        K = wl.bits_to_f32(case.k0, dtype).astype(np.float64)
+        frac = _late_max_fraction(ref, K, w, w.P // 256)
+        assert frac > 0.1, f"the rescale is taken by only {frac:.3f} of the rows"
+        check_prefill(case, out, ref, f"late spikes {dtype}", beyond_rounding=True)
     finally:
         case.free()
 

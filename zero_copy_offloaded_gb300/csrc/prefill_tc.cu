@@ -19,15 +19,16 @@
 //      a complete softmax over the chunk (it is stationary, so there is no
 //      running rescale), O = P.V (tcgen05 with P as the TMEM operand, fp16),
 //      and its normalised O (staged in shared memory, TMA store) and base-2
-//      log-sum-exp are written as the chunk's partial.  S of tile i+1 is
-//      computed while the softmax of tile i runs.
+//      log-sum-exp are written as the chunk's partial.  Two Q tiles are in
+//      flight, each in its own TMEM region, so the tensor cores compute one
+//      tile's S or O while the other tile's softmax or epilogue runs.
 // A combine kernel merges the chunks' partials per query row.
 //
 // Warp roles (320 threads): warp 0 loads (TMA / cp.async), warp 1 allocates
-// TMEM and issues every MMA from one thread, warps 2-9 are the softmax /
-// epilogue warps: two per TMEM lane quarter, each owning half of a row's 256
-// scores (the halves exchange their max and sum through shared memory).
-// Every wait is bounded.
+// TMEM and issues every MMA from one thread, warps 2-9 are two softmax /
+// epilogue groups of four (one warp per TMEM lane quarter, one row per
+// thread): group 0 takes the even Q tiles, group 1 the odd ones.  Every wait
+// is bounded.
 #include "tc_common.cuh"
 
 namespace dkv {
@@ -45,10 +46,13 @@ constexpr int kBQ = 128;       // rows per Q tile
 constexpr int kThreads = 320;  // 10 warps
 constexpr int kRegKV = kC * 128;   // one 256-row x 128-byte swizzled region (K or V)
 constexpr int kRegQ = kBQ * 128;   // one 128-row x 128-byte swizzled region
-// TMEM columns
-constexpr uint32_t kTmS = 0;       // S: 256 fp32 columns
-constexpr uint32_t kTmO = 256;     // O: D fp32 columns
-constexpr uint32_t kTmP = 384;     // P: 256 fp16 keys, two per column
+// TMEM: two regions of 256 columns, one per Q tile in flight (tile i uses
+// region i & 1).  A region holds S (256 fp32 columns); the softmax then writes
+// P (256 fp16 keys, two per column) over columns 0..127 of the consumed
+// scores, and P.V accumulates O (D fp32 columns) in columns 128..128+D-1.
+constexpr uint32_t kTmRegion = 256;
+constexpr uint32_t kTmP = 0;
+constexpr uint32_t kTmO = 128;
 
 template <int D>
 struct TcCfg {
@@ -81,20 +85,17 @@ constexpr int smem_request() {
 }
 
 struct Bars {
-  uint64_t q_full[2], q_empty[2], s_full, s_empty, p_full, p_empty, o_full, o_empty, kv_host,
-      kv_ready, pr_full[2], pr_empty[2], pr_done, pr_drain;
-  // rendezvous of the two warps sharing a TMEM lane quarter (halves of the
-  // same rows): max exchange, last-tile sum exchange, shared staging (D = 64)
-  uint64_t xpair[3][4];
-  // the pair has read the exchange slots (xmax, xl) of a step: one arrival
-  // per warp, waited on only before the slots are written again
-  uint64_t xfree[4];
+  uint64_t q_full[2], q_empty[2], kv_host, kv_ready, pr_full[2], pr_empty[2], pr_done, pr_drain;
+  // per TMEM region: S computed, P written (4 warps), O computed, O read out
+  // (4 warps: the region may take the next tile's S)
+  uint64_t s_full[2], p_full[2], o_full[2], r_free[2];
+  // per lane quarter: the output staging rows were read by the TMA store of
+  // the previous tile (the other group's), one arrival per tile
+  uint64_t st_free[4];
   uint64_t vsync;     // rendezvous of the four warps converting V
   uint32_t tmem_base;
   volatile int abort;
   float vmax[4];
-  float xmax[2][kBQ];  // the two halves' row maxima
-  float xl[2][kBQ];    // the two halves' row sums
 };
 
 struct TcArgs {
@@ -203,19 +204,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->pr_full[i], 1);
       mbar_init(&bars->pr_empty[i], 1);
     }
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_empty, 8);
-    mbar_init(&bars->p_full, 8);
-    mbar_init(&bars->p_empty, 1);
-    mbar_init(&bars->o_full, 1);
-    mbar_init(&bars->o_empty, 8);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&bars->s_full[g], 1);
+      mbar_init(&bars->p_full[g], 4);
+      mbar_init(&bars->o_full[g], 1);
+      mbar_init(&bars->r_free[g], 4);
+    }
+    for (int q = 0; q < 4; ++q) mbar_init(&bars->st_free[q], 1);
     mbar_init(&bars->kv_host, 32);
     mbar_init(&bars->kv_ready, 8);
     mbar_init(&bars->pr_done, 1);
     mbar_init(&bars->pr_drain, 8);
-    for (int i = 0; i < 3; ++i)
-      for (int q = 0; q < 4; ++q) mbar_init(&bars->xpair[i][q], 2);
-    for (int q = 0; q < 4; ++q) mbar_init(&bars->xfree[q], 2);
     mbar_init(&bars->vsync, 4);
     bars->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -326,46 +325,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_s = tc::idesc_f16(bf, 128, kC, false, false);  // Q.K^T, N = 256
       const uint32_t idesc_o = tc::idesc_f16(false, 128, D, false, true); // P.V in fp16
       const uint32_t ka = smem_u32(ks), va = smem_u32(vs);
-      auto issue_s = [&](int i) -> bool {
-        const int s = i & 1;
-        if (!wait_or_abort(&bars->q_full[s], (i >> 1) & 1, bars, a.status, kSiteFull)) return false;
-        // S of tile i-1 has been read by the softmax warps
-        if (!wait_or_abort(&bars->s_empty, (i & 1) ^ 1, bars, a.status, kSiteEmpty)) return false;
-        tc::fence_after_sync();
-        const uint32_t qa = smem_u32(qs + s * Cfg::kQ);
+      // S of tile i into region i & 1 (its Q tile has landed; the region's
+      // previous tile has had its O read out)
+      auto issue_s = [&](int i) {
+        const uint32_t rg = tmem + (uint32_t)(i & 1) * kTmRegion;
+        const uint32_t qa = smem_u32(qs + (i & 1) * Cfg::kQ);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma_ss(tmem + kTmS,
-                     tc::sdesc_sw128(qa + (kk / 4) * kRegQ + (kk % 4) * 32, 16, 1024),
+          tc::mma_ss(rg, tc::sdesc_sw128(qa + (kk / 4) * kRegQ + (kk % 4) * 32, 16, 1024),
                      tc::sdesc_sw128(ka + (kk / 4) * kRegKV + (kk % 4) * 32, 16, 1024), idesc_s,
                      kk != 0);
-        tc::mma_commit(&bars->s_full);
-        tc::mma_commit(&bars->q_empty[s]);
-        return true;
+        tc::mma_commit(&bars->s_full[i & 1]);
+        tc::mma_commit(&bars->q_empty[i & 1]);
       };
-      if (ntiles > 0) issue_s(0);
-      for (int i = 0; i < ntiles && !bars->abort; ++i) {
-        if (i + 1 < ntiles && !issue_s(i + 1)) break;
-        // P of tile i is in TMEM and O has been read out for tile i-1
-        if (!wait_or_abort(&bars->p_full, i & 1, bars, a.status, kSiteFull)) break;
-        if (!wait_or_abort(&bars->o_empty, (i & 1) ^ 1, bars, a.status, kSiteEmpty)) break;
-        tc::fence_after_sync();
+      // O of tile i = P.V, P read from the region's TMEM (fp16), V from shared
+      auto issue_pv = [&](int i) {
+        const uint32_t rg = tmem + (uint32_t)(i & 1) * kTmRegion;
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
-          tc::mma_ts(tmem + kTmO, tmem + kTmP + kk * 8,
+          tc::mma_ts(rg + kTmO, rg + kTmP + kk * 8,
                      tc::sdesc_sw128(va + kk * 2048, kRegKV, 1024), idesc_o, kk != 0);
-        tc::mma_commit(&bars->o_full);
-        tc::mma_commit(&bars->p_empty);
+        tc::mma_commit(&bars->o_full[i & 1]);
+      };
+      // Issue whichever is ready: the next S (tiles in order, at most two in
+      // flight) or the next P.V (in order, once its softmax wrote P).  The
+      // tests never suspend, so a barrier that is not ready cannot hold up one
+      // that is.  Each test is on the phase right after one this thread has
+      // already seen complete, so a parity test cannot mistake an older phase
+      // for it.
+      int ns = 0, np = 0;
+      uint64_t deadline = 0;
+      bool idle = false;
+      while (np < ntiles) {
+        bool did = false;
+        if (ns < ntiles && ns < np + 2 &&
+            mbar_test_wait(&bars->q_full[ns & 1], (ns >> 1) & 1) &&
+            (ns < 2 || mbar_test_wait(&bars->r_free[ns & 1], ((ns - 2) >> 1) & 1))) {
+          tc::fence_after_sync();
+          issue_s(ns++);
+          did = true;
+        }
+        if (np < ns && mbar_test_wait(&bars->p_full[np & 1], (np >> 1) & 1)) {
+          tc::fence_after_sync();
+          issue_pv(np++);
+          did = true;
+        }
+        if (did) {
+          idle = false;
+          continue;
+        }
+        if (bars->abort) break;
+        const uint64_t now = global_timer_ns();
+        if (!idle) {
+          idle = true;
+          deadline = now + kWaitBudgetNs;
+        } else if (now > deadline) {
+          record_timeout(a.status, kSiteFull);
+          bars->abort = 1;
+          break;
+        }
       }
     }
     __syncwarp();
   } else {
     // ============================================= softmax / epilogue warps
-    const int hh = (warp - 2) / 4;            // which half of the 256 scores this warp owns
+    const int hh = (warp - 2) / 4;            // group: K/V half of the projection, tile parity
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;      // tile row = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int hrow = hh * 128 + row;          // this thread's row in a 256-row K/V tile
 
     // (a) projection epilogue per pass: half 0 takes the K columns, half 1
     //     the V columns; round, write into the stationary tile, append.
@@ -453,163 +480,152 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars->kv_ready);
 
-    // (b) the Q tiles: softmax over this half's 128 scores, then the output
-    //     epilogue for this half's D/2 columns
-    (void)hrow;
+    // (b) the Q tiles.  Group hh takes tiles hh, hh + 2, ... in TMEM region
+    //     hh; each thread owns one row (its TMEM lane) and all 256 scores of
+    //     it, so a group needs no exchange beyond its four-warp arrivals.
     const float scale = a.scale_log2;
-    // With D = 128 each warp stores its own 64 output columns of its 32 rows;
-    // with D = 64 the two halves share one 128-byte row and the half-0 warp
-    // stores it.
-    constexpr bool kOwnStore = DR == 2;
-    const bool storer = lane == 0 && (kOwnStore || hh == 0);
     const size_t TG = (size_t)a.T * G;
     const size_t blk = ((size_t)c * a.B + b) * a.Hkv + kvh;
-    // softmax(j): S -> P (TMEM) for tile j; returns this half's row sum and
-    // the row max (scaled) in registers for the epilogue of tile j.  Its
-    // max-exchange rendezvous with the partner warp also publishes the
-    // previous tile's half sums (l_prev) and, through the storer, frees the
-    // output staging for the epilogue of tile j - 1 that follows it.
-    auto softmax = [&](int j, float l_prev, float& l_out, float& m_out) -> bool {
-      const uint32_t ph = j & 1;
-      if (!warp_wait(&bars->s_full, ph, bars, a.status, kSiteFull)) return false;
+    const uint32_t rg = tmem + lane_off + (uint32_t)hh * kTmRegion;
+    // the storer hands its staging rows to the other group once its TMA store
+    // has read them; it checks that while waiting for its next S, where the
+    // warp would wait anyway
+    bool pend = false;
+    for (int j = hh, n = 0; j < ntiles; j += 2, ++n) {
+      const uint32_t ph = n & 1;
+      if (!warp_wait(&bars->s_full[hh], ph, bars, a.status, kSiteFull)) break;
+      if (pend) {
+        tc::bulk_wait_read_all();
+        mbar_arrive(&bars->st_free[quarter]);
+        pend = false;
+      }
       tc::fence_after_sync();
       const int t_first = t_lo + j * TQ;
       // every key of the chunk is visible to every row of this tile
       const bool full = nkeys == kC && P + t_first >= k0 + kC - 1;
       const int t = t_first + row / G;
-      const int nvis = min(nkeys, P + t - k0 + 1) - hh * 128;  // visible keys in this half
-      uint32_t r[128];
-#pragma unroll
-      for (int part = 0; part < 4; ++part)
-        tc::tmem_ld32(tmem + lane_off + kTmS + hh * 128 + part * 32,
-                      *reinterpret_cast<uint32_t(*)[32]>(r + part * 32));
-      tc::tmem_wait_ld();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_empty);  // S may be overwritten by tile j + 1
-      float m8[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) m8[q] = -INFINITY;
-      if (full) {
-#pragma unroll
-        for (int k2 = 0; k2 < 128; ++k2) m8[k2 % 8] = fmaxf(m8[k2 % 8], __uint_as_float(r[k2]));
-      } else {
-#pragma unroll
-        for (int k2 = 0; k2 < 128; ++k2)
-          if (k2 < nvis) m8[k2 % 8] = fmaxf(m8[k2 % 8], __uint_as_float(r[k2]));
-      }
-      // the partner has read the slots of the previous step (its xmax of
-      // tile j - 1 and xl of tile j - 2) before they are overwritten
-      if (j > 0 && !warp_wait(&bars->xfree[quarter], (j - 1) & 1, bars, a.status, kSiteEmpty))
-        return false;
-      bars->xmax[hh][row] = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                  fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      if (j > 0) {
-        bars->xl[hh][row] = l_prev;
-        if (storer) tc::bulk_wait_read_all();  // tile j-2's stores left the staging
-      }
-      if (!warps_sync(&bars->xpair[0][quarter], ph, bars, a.status)) return false;
-      const float mx = fmaxf(bars->xmax[0][row], bars->xmax[1][row]) * scale;
-      if (j == 0) {  // step 0 of the exchange slots is read
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->xfree[quarter]);
-      }
-      // P = 2^(s*scale - m) in fp16 (l sums the weights before the rounding:
-      // the normalisation then differs from the rounded weights' sum by at
-      // most 2^-12 relative).  The weights are formed in registers while the
-      // P.V of tile j - 1 still reads the previous P from TMEM; only the
-      // stores into TMEM wait for it.
+      const int nvis = min(nkeys, P + t - k0 + 1);  // keys [0, nvis) are visible to this row
+      // P = 2^(s*scale - m) in fp16, 64 keys at a time, written over scores
+      // this thread has already read (keys 2c, 2c+1 in column c).  m is the
+      // max of the first 64 visible scores; later scores may exceed it by up
+      // to 2^15 (fp16 P and the fp32 sums hold that).  A piece that exceeds
+      // it by more takes its own max as m and rescales the weights already
+      // written, so no weight ends up less precise than with the exact max.
+      // l sums the weights before the rounding: the normalisation then
+      // differs from the rounded weights' sum by at most 2^-12 relative.
+      constexpr float kHeadroom = 15.f;
+      float mx = -INFINITY;
       float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      uint32_t w[64];
+#pragma unroll 1
+      for (int pc = 0; pc < kC / 64; ++pc) {
+        uint32_t r[64];
+        tc::tmem_ld32(rg + pc * 64, *reinterpret_cast<uint32_t(*)[32]>(r));
+        tc::tmem_ld32(rg + pc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+        tc::tmem_wait_ld();
+        // piece max (for piece 0 the reference m; for later pieces only the
+        // headroom check, so it runs alongside the exponentials)
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (full) {
 #pragma unroll
-      for (int e = 0; e < 64; ++e) {
-        const int k2 = 2 * e;
-        float p0 = tc::ex2_approx(fmaf(__uint_as_float(r[k2]), scale, -mx));
-        float p1 = tc::ex2_approx(fmaf(__uint_as_float(r[k2 + 1]), scale, -mx));
-        if (!full) {
-          p0 = k2 < nvis ? p0 : 0.f;
-          p1 = k2 + 1 < nvis ? p1 : 0.f;
+          for (int k2 = 0; k2 < 64; ++k2) m4[k2 % 4] = fmaxf(m4[k2 % 4], __uint_as_float(r[k2]));
+        } else {
+#pragma unroll
+          for (int k2 = 0; k2 < 64; ++k2)
+            if (pc * 64 + k2 < nvis) m4[k2 % 4] = fmaxf(m4[k2 % 4], __uint_as_float(r[k2]));
         }
-        w[e] = tc::pack2<__half>(p0, p1);
-        l8[(2 * e) % 8] += p0;
-        l8[(2 * e + 1) % 8] += p1;
+        const float pm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale;
+        if (pc == 0) mx = pm;
+        uint32_t w[32];
+        float ls8[8];
+        auto weights = [&]() {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) ls8[q] = 0.f;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int k2 = pc * 64 + 2 * e;
+            float p0 = tc::ex2_approx(fmaf(__uint_as_float(r[2 * e]), scale, -mx));
+            float p1 = tc::ex2_approx(fmaf(__uint_as_float(r[2 * e + 1]), scale, -mx));
+            if (!full) {
+              p0 = k2 < nvis ? p0 : 0.f;
+              p1 = k2 + 1 < nvis ? p1 : 0.f;
+            }
+            w[e] = tc::pack2<__half>(p0, p1);
+            ls8[(2 * e) % 8] += p0;
+            ls8[(2 * e + 1) % 8] += p1;
+          }
+        };
+        weights();
+        if (pc > 0) {
+          const bool need = pm > mx + kHeadroom;
+          if (__any_sync(0xffffffffu, need)) {  // rare; TMEM access is warp-wide
+            const float f = need ? tc::ex2_approx(mx - pm) : 1.f;
+            tc::tmem_wait_st();
+            for (int q = 0; q < pc; ++q) {
+              uint32_t v2[32];
+              tc::tmem_ld32(rg + kTmP + q * 32, v2);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&v2[e]));
+                v2[e] = tc::pack2<__half>(v.x * f, v.y * f);
+              }
+              tc::tmem_st32(rg + kTmP + q * 32, v2);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) l8[q] *= f;
+            if (need) mx = pm;
+            weights();  // this piece again, against the new m
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) l8[q] += ls8[q];
+        tc::tmem_st32(rg + kTmP + pc * 32, w);
       }
-      if (!warp_wait(&bars->p_empty, ph ^ 1, bars, a.status, kSiteEmpty)) return false;
-      tc::tmem_st32(tmem + lane_off + kTmP + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(w));
-      tc::tmem_st32(tmem + lane_off + kTmP + hh * 64 + 32,
-                    *reinterpret_cast<uint32_t(*)[32]>(w + 32));
       tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full);  // P is ready for the P.V MMA
-      l_out = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
-      m_out = mx;
-      return true;
-    };
-    // epilogue(j): O / l in fp16 staged in shared memory, written with TMA
-    // stores; the base-2 lse with plain stores.  Both land tile-contiguous:
-    // block (c, b, kvh), rows (t, g).
-    auto epilogue = [&](int j, float l_half, float mx, bool last) -> bool {
-      const uint32_t ph = j & 1;
-      const int t_first = t_lo + j * TQ;
-      const int t = t_first + row / G;
-      if (!warp_wait(&bars->o_full, ph, bars, a.status, kSiteFull)) return false;
+      if (lane == 0) mbar_arrive(&bars->p_full[hh]);  // P is ready for the P.V MMA
+      const float l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+
+      // epilogue: O / l in fp16 staged in shared memory and written with TMA
+      // stores, the base-2 lse with plain stores; both land tile-contiguous:
+      // block (c, b, kvh), rows (t, g)
+      if (!warp_wait(&bars->o_full[hh], ph, bars, a.status, kSiteFull)) break;
       tc::fence_after_sync();
-      if (last) {  // no later softmax published the half sums: rendezvous here
-        if (!warp_wait(&bars->xfree[quarter], j & 1, bars, a.status, kSiteEmpty)) return false;
-        bars->xl[hh][row] = l_half;
-        if (storer) tc::bulk_wait_read_all();
-        if (!warps_sync(&bars->xpair[1][quarter], 0, bars, a.status)) return false;
-      }
-      const float l = bars->xl[0][row] + bars->xl[1][row];
-      if (!last) {  // step j + 1 of the exchange slots is read
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->xfree[quarter]);
-      }
-      constexpr int DH = D / 2;  // output columns per half
-      uint32_t r[DH];
+      uint32_t o[D];
 #pragma unroll
-      for (int part = 0; part < DH / 32; ++part)
-        tc::tmem_ld32(tmem + lane_off + kTmO + hh * DH + part * 32,
-                      *reinterpret_cast<uint32_t(*)[32]>(r + part * 32));
+      for (int part = 0; part < D / 32; ++part)
+        tc::tmem_ld32(rg + kTmO + part * 32, *reinterpret_cast<uint32_t(*)[32]>(o + part * 32));
       tc::tmem_wait_ld();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->o_empty);  // O may be overwritten by tile j + 1
+      if (lane == 0) mbar_arrive(&bars->r_free[hh]);  // the region may take tile j + 2
       const float inv = 1.f / l;
+      // the staging rows of this quarter have been read by tile j - 1's store
+      if (j > 0 && !warp_wait(&bars->st_free[quarter], (j - 1) & 1, bars, a.status, kSiteEmpty))
+        break;
 #pragma unroll
-      for (int q = 0; q < DH / 8; ++q)
-        *reinterpret_cast<uint4*>(os + swz(row, hh * (DH / 8) + q, kRegQ)) =
-            pack8<__half>(r + q * 8, inv);
-      if (hh == 0 && t < a.T) a.part_lse[blk * TG + (size_t)t * G + row % G] = mx + log2f(l);
+      for (int q = 0; q < D / 8; ++q)
+        *reinterpret_cast<uint4*>(os + swz(row, q, kRegQ)) = pack8<__half>(o + q * 8, inv);
+      if (t < a.T) a.part_lse[blk * TG + (size_t)t * G + row % G] = mx + log2f(l);
       tc::fence_proxy_async_smem();
-      const int row0 = t_first * G + quarter * 32;  // rows past T*G are clipped by the store
-      if constexpr (!kOwnStore) {
-        if (!warps_sync(&bars->xpair[2][quarter], ph, bars, a.status)) return false;
-      } else {
-        __syncwarp();
+      __syncwarp();
+      if (lane == 0) {
+        const int row0 = t_first * G + quarter * 32;  // rows past T*G are clipped by the store
+        if (row0 < (int)TG) {
+#pragma unroll
+          for (int rr = 0; rr < DR; ++rr)
+            tc::tma_store_3d(&map_po, rr * 64, row0, (int)blk, os + rr * kRegQ + quarter * 32 * 128);
+          tc::bulk_commit();
+        }
       }
-      if (storer && row0 < (int)TG) {
-        const int rg = kOwnStore ? hh : 0;
-        tc::tma_store_3d(&map_po, rg * 64, row0, (int)blk, os + rg * kRegQ + quarter * 32 * 128);
-        tc::bulk_commit();
-      }
-      return true;
-    };
-    // softmax of tile i+1 runs before the epilogue of tile i, so the P.V of
-    // tile i proceeds on the tensor cores meanwhile
-    float l_cur = 0.f, m_cur = 0.f;
-    if (softmax(0, 0.f, l_cur, m_cur)) {
-      for (int i = 0; i < ntiles; ++i) {
-        float l_next = 0.f, m_next = 0.f;
-        const bool last = i + 1 == ntiles;
-        if (!last && !softmax(i + 1, l_cur, l_next, m_next)) break;
-        if (!epilogue(i, l_cur, m_cur, last)) break;
-        l_cur = l_next;
-        m_cur = m_next;
-      }
+      pend = lane == 0;
     }
-    if (storer) tc::bulk_wait_all();
+    if (pend) {
+      tc::bulk_wait_read_all();
+      mbar_arrive(&bars->st_free[quarter]);
+    }
+    if (lane == 0) tc::bulk_wait_all();
   }
 
   tc::fence_before_sync();
