@@ -333,6 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
         // (the test hook withholds the first tile's signal: the consumers'
         // bounded wait then expires and reports a timeout)
         if (!(p.debug_withhold && it == 0)) cp_async_arrive_noinc(&full[stage]);
+        // One tile in flight per producer thread (32 KB per SM keeps the link
+        // busy): thousands of outstanding host requests would otherwise hold
+        // up the projection's weight loads on the same load/store path.
+        cp_async_commit();
+        cp_async_wait_group<0>();
       }
     }
     cp_async_wait_all();
