@@ -348,14 +348,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
   const int ctid = tid;
   const int warp = ctid / 32, lane = ctid % 32;
 
-  // Phase A: projection slice of this CTA.
+  // Phase A: projection slice of this CTA.  Columns go out in blocks of
+  // kProjCols (whole 128-byte lines of every weight row) when there are enough
+  // blocks to occupy at least half of the CTAs; narrower projections spread
+  // 8-column bands over every CTA instead.  (Narrow strided pieces of each
+  // row made the weight loads, not the FMA chains, phase A's pace.)
   if (p.mode != kDecodeAttendOnly) {
     const int ncol = (p.Hq + 2 * p.Hkv) * D;
-    const int nblk = ncol / 8;
-    const int per = nblk / gridDim.x, rem = nblk % gridDim.x;
-    const int b0 = blockIdx.x * per + min((int)blockIdx.x, rem);
-    const int b1 = b0 + per + ((int)blockIdx.x < rem ? 1 : 0);
-    if (b1 > b0) project_columns<T, C, D>(p, b0 * 8, b1 * 8, smem, L, ctid);
+    const int nwide = (ncol + kProjCols - 1) / kProjCols;
+    if (2 * nwide >= (int)gridDim.x) {
+      for (int bi = blockIdx.x; bi < nwide; bi += gridDim.x)
+        project_columns<T, C, D>(p, bi * kProjCols, min(ncol, (bi + 1) * kProjCols), smem, L,
+                                 ctid);
+    } else {
+      const int nblk = ncol / 8;
+      const int per = nblk / gridDim.x, rem = nblk % gridDim.x;
+      const int b0 = blockIdx.x * per + min((int)blockIdx.x, rem);
+      const int b1 = b0 + per + ((int)blockIdx.x < rem ? 1 : 0);
+      if (b1 > b0) project_columns<T, C, D>(p, b0 * 8, b1 * 8, smem, L, ctid);
+    }
   }
   if (p.mode == kDecodeProjectOnly) return;  // the producers returned at once
   if (p.mode == kDecodeFused) {
