@@ -212,6 +212,13 @@ def sweep(args, dkv, torch, dev, stream, flush, pk):
     hbm = pk.get("hbm_gbs") or 6800.0
     print(json.dumps({"sweep": "link", "zero_copy_read_gbs": link_rd,
                       "zero_copy_write_gbs": link_wr}), flush=True)
+    # the fp64 oracle on the tiny decode workload, on every core and on one
+    tw = wl.WORKLOADS["tiny_decode"]
+    oracle_decode_sample(tw)  # builds / loads the oracle outside the timing
+    t_all, cores = min(oracle_decode_sample(tw) for _ in range(3))
+    t_one, _ = min(oracle_decode_sample(tw, threads=1) for _ in range(3))
+    print(json.dumps({"sweep": "oracle_tiny_decode", "kind": "oracle", "tok_s_all_cores": 1 / t_all,
+                      "cores": cores, "tok_s_one_core": 1 / t_one}), flush=True)
     for name, w in wl.WORKLOADS.items():
         if w.phase != "decode":
             continue
@@ -365,10 +372,11 @@ def host_cores():
 
 
 # ---------------------------------------------------------------- oracle
-def oracle_decode_sample(w: wl.Workload, seqs: int = 1):
-    """Time the fp64 oracle on `seqs` sequences of the decode workload."""
+def oracle_decode_sample(w: wl.Workload, seqs: int = 1, threads: int = 0):
+    """Time the fp64 oracle on `seqs` sequences of the decode workload, on
+    `threads` host threads (0: every core in the affinity mask)."""
     import oracle
-    oracle.set_threads(host_cores())
+    oracle.set_threads(threads or host_cores())
     d = wl.make_dense(w.with_(B=seqs))
     k = np.zeros((seqs, w.Hkv, w.S_max, w.D), np.uint16)
     v = np.zeros_like(k)
