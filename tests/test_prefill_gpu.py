@@ -60,8 +60,10 @@ def test_prefill_shapes(dtype, D, Hq, Hkv, P, T):
 def _late_max_fraction(ref, K, w, nchunks):
     """Fraction of (query row, prefix chunk) pairs whose scores past the
     chunk's first 64 keys exceed the max of those 64 by more than 2^15 in
-    weight: the pairs where the fused kernel rescales the weights it has
-    already written (computed from the oracle's q, in fp64)."""
+    weight (computed from the oracle's q, in fp64).  Each such pair makes the
+    fused kernel rescale the weights it has already written (it does so once a
+    64-key piece's weights sum to more than 2^14), so this is a lower bound on
+    how often the rescale runs."""
     q = wl.bits_to_f32(ref["q"], w.dtype).astype(np.float64)  # [B,T,Hq,D]
     G = w.Hq // w.Hkv
     hits = total = 0
@@ -99,11 +101,11 @@ def test_prefill_late_key_spikes(dtype):
     """The key at offset 200 of every 256-key chunk scaled by 40.
 
     The fused kernel forms a row's weights against the max of the chunk's
-    first 64 scores and, when a later score exceeds that max by more than
-    2^15 in weight, rescales the weights it has written and continues
-    against the new max.  Here that happens for a known share of the rows
-    (asserted from the oracle's q), and the outputs are compared with the
-    oracle as everywhere else."""
+    first 64 scores and, when a later 64-key piece's weights sum to more than
+    2^14, rescales the weights it has written and continues against that
+    piece's max.  Here that happens for a known share of the rows (bounded
+    below from the oracle's q), and the outputs are compared with the oracle
+    as everywhere else."""
     w = wl.Workload("t", "prefill", B=2, H=128, Hq=8, Hkv=2, D=128, P=768, T=64, dtype=dtype,
                     kv_dist="uniform2" if dtype == "fp16" else "normal", seed=23)
     case = Case(w, s_max=w.P + w.T + 3)

@@ -507,13 +507,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nvis = min(nkeys, P + t - k0 + 1);  // keys [0, nvis) are visible to this row
       // P = 2^(s*scale - m) in fp16, 64 keys at a time, written over scores
       // this thread has already read (keys 2c, 2c+1 in column c).  m is the
-      // max of the first 64 visible scores; later scores may exceed it by up
-      // to 2^15 (fp16 P and the fp32 sums hold that).  A piece that exceeds
-      // it by more takes its own max as m and rescales the weights already
-      // written, so no weight ends up less precise than with the exact max.
-      // l sums the weights before the rounding: the normalisation then
-      // differs from the rounded weights' sum by at most 2^-12 relative.
-      constexpr float kHeadroom = 15.f;
+      // max of the first 64 visible scores.  A later piece whose weights sum
+      // to at most 2^14 has none above 2^14, which fp16 P and the fp32 sums
+      // hold; one that sums to more (a score more than 8 above m, or an
+      // overflow) takes its own max as m and rescales the weights already
+      // written.  So m never exceeds the row max (the largest weight is >= 1)
+      // and no weight ends up less precise than with the exact max.  l sums
+      // the weights before the rounding: the normalisation then differs from
+      // the rounded weights' sum by at most 2^-12 relative.
+      constexpr float kSumBound = 16384.f;
       float mx = -INFINITY;
       float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
@@ -522,19 +524,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_ld32(rg + pc * 64, *reinterpret_cast<uint32_t(*)[32]>(r));
         tc::tmem_ld32(rg + pc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
         tc::tmem_wait_ld();
-        // piece max (for piece 0 the reference m; for later pieces only the
-        // headroom check, so it runs alongside the exponentials)
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (full) {
+        // max of the piece's visible scores (scaled): the reference m for the
+        // first piece, and in the rare rescale below
+        auto piece_max = [&]() {
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          if (full) {
 #pragma unroll
-          for (int k2 = 0; k2 < 64; ++k2) m4[k2 % 4] = fmaxf(m4[k2 % 4], __uint_as_float(r[k2]));
-        } else {
+            for (int k2 = 0; k2 < 64; ++k2)
+              m4[k2 % 4] = fmaxf(m4[k2 % 4], __uint_as_float(r[k2]));
+          } else {
 #pragma unroll
-          for (int k2 = 0; k2 < 64; ++k2)
-            if (pc * 64 + k2 < nvis) m4[k2 % 4] = fmaxf(m4[k2 % 4], __uint_as_float(r[k2]));
-        }
-        const float pm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale;
-        if (pc == 0) mx = pm;
+            for (int k2 = 0; k2 < 64; ++k2)
+              if (pc * 64 + k2 < nvis) m4[k2 % 4] = fmaxf(m4[k2 % 4], __uint_as_float(r[k2]));
+          }
+          return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale;
+        };
+        if (pc == 0) mx = piece_max();
         uint32_t w[32];
         float ls8[8];
         auto weights = [&]() {
@@ -556,8 +561,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         weights();
         if (pc > 0) {
-          const bool need = pm > mx + kHeadroom;
+          const float ls = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+          const bool need = !(ls <= kSumBound);  // also an inf or NaN sum
           if (__any_sync(0xffffffffu, need)) {  // rare; TMEM access is warp-wide
+            const float pm = need ? piece_max() : mx;
             const float f = need ? tc::ex2_approx(mx - pm) : 1.f;
             tc::tmem_wait_st();
             for (int q = 0; q < pc; ++q) {
@@ -573,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int q = 0; q < 8; ++q) l8[q] *= f;
-            if (need) mx = pm;
+            mx = pm;
             weights();  // this piece again, against the new m
           }
         }
