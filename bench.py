@@ -302,7 +302,7 @@ def ncu_traffic(key, files):
     kernel sources as they are now (else None)."""
     try:
         rec = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))[key]
-    except Exception:
+    except (OSError, ValueError, KeyError):
         return None
     return rec if rec.get("src_sha256_16") == kernel_source_hash(files) else None
 
@@ -310,7 +310,7 @@ def ncu_traffic(key, files):
 def peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
-    except Exception:
+    except (OSError, ValueError):
         return {}
 
 
@@ -332,7 +332,7 @@ class Clocks:
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
-        except Exception:
+        except OSError:  # no nvidia-smi on this machine
             self.proc = None
 
     def stop(self):
@@ -342,7 +342,7 @@ class Clocks:
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
-        except Exception:
+        except subprocess.TimeoutExpired:
             self.proc.kill()
         self.f.flush()
         rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r.strip()]
@@ -356,7 +356,7 @@ class Clocks:
                 for n, v in zip(names, r[5:9]):
                     if v.strip().lower() == "active":
                         reasons.add(n)
-            except Exception:
+            except (ValueError, IndexError):  # a partial or non-numeric line
                 continue
         if not sm:
             return None
@@ -367,7 +367,7 @@ class Clocks:
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
-    except Exception:
+    except (AttributeError, OSError):
         return os.cpu_count() or 1
 
 
