@@ -116,8 +116,8 @@ dkv_status dkv_cache_alloc(dkv_cache** out, int batch, int n_kv_heads, int head_
 /* The general allocator behind dkv_cache_alloc, dkv_cache_alloc_layered and
  * dkv_cache_alloc_paged, which also takes the element format.  An E4M3 cache
  * serves dkv_decode / dkv_decode_layer / dkv_decode_unfused / captured steps
- * (its host views hold uint8 E4M3 bits); dkv_prefill, dkv_decode_staged and
- * dkv_attend_naive return UNSUPPORTED for it.  Errors: as the three
+ * (its host views hold uint8 E4M3 bits); dkv_prefill, dkv_decode_staged,
+ * dkv_prefill_staged and dkv_attend_naive return UNSUPPORTED for it.  Errors: as the three
  * allocators, plus INVALID_ARG for an unknown format, UNSUPPORTED for E4M3
  * with fp16 activations or a paged cache of several layers. */
 dkv_status dkv_cache_alloc_ex(dkv_cache** out, const dkv_cache_desc_t* desc);
@@ -322,6 +322,18 @@ dkv_status dkv_decode_unfused(dkv_cache* cache, const void* x, const void* wq, c
 dkv_status dkv_decode_staged(dkv_cache* cache, const void* x, const void* wq, const void* wk,
                              const void* wv, int hidden, int n_q_heads, void* out,
                              void* k_stage, void* v_stage, void* stream);
+
+/* The same baseline for prefill: cudaMemcpyAsync the cached rows [0, len[b])
+ * of every (sequence, KV head) into the caller's HBM buffers k_stage,
+ * v_stage (each [B][Hkv][max_tokens][D], device memory the caller owns), then
+ * run the same fused prefill as dkv_prefill reading the cached prefix from
+ * HBM; the T new rows are still appended to the host cache and the lengths
+ * advance by T.  Same arguments, results and errors as dkv_prefill, plus
+ * INVALID_ARG for a null staging buffer and UNSUPPORTED for a paged, layered
+ * or E4M3 cache. */
+dkv_status dkv_prefill_staged(dkv_cache* cache, const void* x, int T, const void* wq,
+                              const void* wk, const void* wv, int hidden, int n_q_heads,
+                              void* out, void* k_stage, void* v_stage, void* stream);
 
 /* Kernel timing for measurement: when enabled, each dkv_decode / dkv_prefill
  * records a pair of CUDA events on its stream around its main fused kernel

@@ -10,9 +10,10 @@ untouched."""
 import numpy as np
 import pytest
 
+import zero_copy_offloaded_gb300 as dkv
 from zero_copy_offloaded_gb300 import workloads as wl
 
-from .helpers import (Case, assert_close, assert_close_beyond_rounding, assert_projection_close,
+from .helpers import (Case, torch_dtype, assert_close, assert_close_beyond_rounding, assert_projection_close,
                       out_f64)
 
 pytestmark = pytest.mark.gpu
@@ -165,6 +166,50 @@ def test_prefill_then_decode_matches_oracle():
         assert_close(got, ref2["out"].reshape(w.B, w.Hq, w.D), "decode after prefill")
     finally:
         case.free()
+
+
+def test_prefill_staged_baseline():
+    """The copy-to-HBM baseline: the cached prefix is copied into HBM buffers
+    and the same fused prefill reads it from there.  Against the oracle as
+    every prefill, and bit-identical to the zero-copy prefill of the same
+    inputs (the same kernel over the same values); refusals for a missing
+    staging buffer and a paged cache."""
+    import torch
+    w = wl.Workload("t", "prefill", B=2, H=128, Hq=8, Hkv=2, D=128, P=300, T=70, seed=37)
+    case = Case(w, lens=[300, 45], s_max=380)
+    try:
+        n = w.B * w.Hkv * case.s_max * w.D
+        k_stage = torch.zeros(n, dtype=torch_dtype(w.dtype), device="cuda")
+        v_stage = torch.zeros_like(k_stage)
+        out_s = case.out_tensor(w.T)
+        dkv.dkv_prefill_staged(case.cache.h, case.x, w.T, case.wq, case.wk, case.wv, w.H, w.Hq,
+                               out_s, k_stage, v_stage, None)
+        case.cache.sync()
+        ref = case.oracle()
+        check_prefill(case, out_s, ref, "staged prefill")
+        # the zero-copy prefill on the same caches (reset) gives the same bits
+        case.cache.k_host[...] = case.k0
+        case.cache.v_host[...] = case.v0
+        case.cache.set_lengths(case.lens.astype(np.int32))
+        out_z = case.run_prefill()
+        assert torch.equal(out_s.view(torch.int16), out_z.view(torch.int16))
+        case.cache.set_lengths(case.lens.astype(np.int32))  # room for T more rows
+        with pytest.raises(dkv.DkvError) as ei:
+            dkv.dkv_prefill_staged(case.cache.h, case.x, w.T, case.wq, case.wk, case.wv, w.H,
+                                   w.Hq, out_s, None, v_stage, None)
+        assert ei.value.name == "DKV_ERR_INVALID_ARG"
+    finally:
+        case.free()
+    pw = wl.Workload("t", "prefill", B=1, H=128, Hq=8, Hkv=2, D=64, P=20, T=8, seed=3)
+    pc = Case(pw, s_max=32, page_tokens=16)
+    try:
+        st = torch.zeros(1 << 16, dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(dkv.DkvError) as ei:
+            dkv.dkv_prefill_staged(pc.cache.h, pc.x, pw.T, pc.wq, pc.wk, pc.wv, pw.H, pw.Hq,
+                                   pc.out_tensor(pw.T), st, st, None)
+        assert ei.value.name == "DKV_ERR_UNSUPPORTED"
+    finally:
+        pc.free()
 
 
 @pytest.mark.slow

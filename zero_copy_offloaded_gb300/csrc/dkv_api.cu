@@ -806,17 +806,15 @@ dkv_status dkv_decode_staged(dkv_cache* c, const void* x, const void* wq, const 
   return decode_impl(c, x, wq, wk, wv, hidden, n_q_heads, out, k_stage, v_stage, s);
 }
 
-dkv_status dkv_prefill_layer(dkv_cache* c, int layer, const void* x, int T, const void* wq,
-                             const void* wk, const void* wv, int hidden, int n_q_heads, void* out,
-                             void* stream) {
-  dkv_status st = check_call(c, x, wq, wk, wv, hidden, n_q_heads, out, T);
-  if (st != DKV_OK) return st;
-  if (layer < 0 || layer >= c->layers)
-    return fail(DKV_ERR_INVALID_ARG, "layer %d outside [0, %d)", layer, c->layers);
-  if (c->kv_format != DKV_KV_NATIVE)
-    return fail(DKV_ERR_UNSUPPORTED, "prefill needs a 16-bit cache (E4M3 caches serve decode)");
-  std::lock_guard<std::mutex> lk(c->mu);
-  if ((st = set_device(c)) != DKV_OK) return st;
+namespace {
+
+// Shared by dkv_prefill_layer and dkv_prefill_staged: the cached rows are read
+// from k_read / v_read (the host cache, or an HBM copy of it), the new rows
+// are appended to the host cache.  Called with the cache's mutex held.
+dkv_status prefill_impl(dkv_cache* c, int layer, const void* x, int T, const void* wq,
+                        const void* wk, const void* wv, int hidden, int n_q_heads, void* out,
+                        const void* k_read, const void* v_read, void* stream) {
+  dkv_status st;
   const int G = n_q_heads / c->Hkv;
   if (!prefill_supported(c->dtype, c->D, G))
     return fail(DKV_ERR_UNSUPPORTED, "no prefill kernel for dtype=%d D=%d G=%d", c->dtype, c->D, G);
@@ -836,8 +834,8 @@ dkv_status dkv_prefill_layer(dkv_cache* c, int layer, const void* x, int T, cons
   memset(&p, 0, sizeof p);
   p.x = x; p.wk = wk; p.wv = wv; p.q = w;
   const size_t loff = (size_t)layer * c->layer_elems * 2;  // bytes
-  p.k_read = static_cast<char*>(c->k_dev) + loff;
-  p.v_read = static_cast<char*>(c->v_dev) + loff;
+  p.k_read = static_cast<const char*>(k_read) + loff;
+  p.v_read = static_cast<const char*>(v_read) + loff;
   p.k_host = static_cast<char*>(c->k_dev) + loff;
   p.v_host = static_cast<char*>(c->v_dev) + loff;
   p.part_o = w + q_b;
@@ -864,6 +862,51 @@ dkv_status dkv_prefill_layer(dkv_cache* c, int layer, const void* x, int T, cons
     c->len_dev_stale = true;
   }
   return DKV_OK;
+}
+
+}  // namespace
+
+dkv_status dkv_prefill_layer(dkv_cache* c, int layer, const void* x, int T, const void* wq,
+                             const void* wk, const void* wv, int hidden, int n_q_heads, void* out,
+                             void* stream) {
+  dkv_status st = check_call(c, x, wq, wk, wv, hidden, n_q_heads, out, T);
+  if (st != DKV_OK) return st;
+  if (layer < 0 || layer >= c->layers)
+    return fail(DKV_ERR_INVALID_ARG, "layer %d outside [0, %d)", layer, c->layers);
+  if (c->kv_format != DKV_KV_NATIVE)
+    return fail(DKV_ERR_UNSUPPORTED, "prefill needs a 16-bit cache (E4M3 caches serve decode)");
+  std::lock_guard<std::mutex> lk(c->mu);
+  if ((st = set_device(c)) != DKV_OK) return st;
+  return prefill_impl(c, layer, x, T, wq, wk, wv, hidden, n_q_heads, out, c->k_dev, c->v_dev,
+                      stream);
+}
+
+dkv_status dkv_prefill_staged(dkv_cache* c, const void* x, int T, const void* wq,
+                              const void* wk, const void* wv, int hidden, int n_q_heads,
+                              void* out, void* k_stage, void* v_stage, void* stream) {
+  dkv_status st = check_call(c, x, wq, wk, wv, hidden, n_q_heads, out, T);
+  if (st != DKV_OK) return st;
+  if (!k_stage || !v_stage) return fail(DKV_ERR_INVALID_ARG, "null staging buffer");
+  if (c->page_tokens || c->layers != 1 || c->kv_format != DKV_KV_NATIVE)
+    return fail(DKV_ERR_UNSUPPORTED, "staged prefill needs a dense one-layer 16-bit cache");
+  std::lock_guard<std::mutex> lk(c->mu);
+  if ((st = set_device(c)) != DKV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t head_elems = (size_t)c->max_tokens * c->D;
+  for (int b = 0; b < c->B; ++b)
+    for (int h = 0; h < c->Hkv; ++h) {
+      const size_t off = ((size_t)b * c->Hkv + h) * head_elems * 2;
+      const size_t n = (size_t)c->len[b] * c->D * 2;
+      if (n == 0) continue;
+      cudaError_t e = cudaMemcpyAsync(static_cast<char*>(k_stage) + off,
+                                      static_cast<char*>(c->k_host) + off, n,
+                                      cudaMemcpyHostToDevice, s);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(static_cast<char*>(v_stage) + off,
+                            static_cast<char*>(c->v_host) + off, n, cudaMemcpyHostToDevice, s);
+      if (e != cudaSuccess) return cuda_fail(e, "staging cudaMemcpyAsync");
+    }
+  return prefill_impl(c, 0, x, T, wq, wk, wv, hidden, n_q_heads, out, k_stage, v_stage, stream);
 }
 
 dkv_status dkv_prefill(dkv_cache* c, const void* x, int T, const void* wq, const void* wk,
