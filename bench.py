@@ -709,6 +709,8 @@ def bench_prefill(args, dkv, torch, dev, stream, flush, pk, link_rd, link_wr, hb
     info = dkv.dkv_cache_info(cache.h)
     cache.free()
     ms = statistics.mean(times)
+    tr = ncu_traffic(f"prefill_tc_kernel/{w.name}", ["prefill_tc.cu", "dkv_internal.cuh",
+                                                      "tc_common.cuh"])
     flops = w.flops()
     tflops_peak = pk.get("bf16_tflops") or 1900.0
     t_link_rd = w.host_read_bytes() / (link_rd * 1e9)
@@ -723,6 +725,11 @@ def bench_prefill(args, dkv, torch, dev, stream, flush, pk, link_rd, link_wr, hb
                                   "hbm": t_hbm * 1e3, "tensor": t_flop * 1e3},
             "frac_of_roofline": t_roof / (ms * 1e-3),
             "copy_to_hbm_then_prefill_ms": statistics.mean(staged),
+            # DRAM bytes of one fused launch and of the combine, from a committed ncu
+            # capture of the current sources (None once they change)
+            "traffic_dram": tr["dram_bytes"] if tr else None,
+            "traffic_dram_combine": (tr["combine_dram_read_bytes"] + tr["combine_dram_write_bytes"]
+                                     if tr else None),
             "hbm_staging_bytes": 2 * nstage * 2,
             "tensor_peak_tflops": tflops_peak,
             "device_workspace_bytes": info["device_workspace_bytes"]}
