@@ -25,11 +25,13 @@
 // The same kernel also runs the two halves of the separate-kernel baseline
 // (DecodeMode): phase A alone, then phase B over rows that all come from the
 // host cache, the freshly appended one included.
-#include "dkv_internal.cuh"
+#include "tc_common.cuh"
 
 #include <cuda_fp8.h>
 
 namespace dkv {
+bool make_tmap_2d_plain(CUtensorMap* map, const void* base, int dtype, uint64_t rows,
+                        uint64_t cols, uint32_t box_cols, uint32_t box_rows);
 namespace {
 
 // Cache element C: the activation type T itself (2 bytes), or 8-bit E4M3
@@ -93,7 +95,7 @@ constexpr int kSmemCap = 232448 - 1024;  // dynamic shared memory per CTA, with 
 // 2) as fit beside the tile ring: the in-order FMA chains wait on one chunk
 // at a time, so deeper staging keeps more HBM loads in flight.
 struct DecodeSmem {
-  int ring, bars, q, s, alpha, ml, red, wproj, xproj, flag, total, proj_stages;
+  int ring, bars, q, s, alpha, ml, red, wproj, xproj, flag, total, proj_stages, pbar;
   int eb;  // bytes per cache element
   __host__ __device__ DecodeSmem(int D, int G, int N, int stages, int B, int eb_ = 2) : eb(eb_) {
     for (proj_stages = 4; proj_stages > 2; --proj_stages)
@@ -111,7 +113,9 @@ struct DecodeSmem {
     ml = off; off += 2 * G * 4;
     red = off; off += kConsumers * 2 * 4;
     off = (off + 15) & ~15;
+    off = (off + 127) & ~127;
     wproj = off; off += proj_stages * kProjRows * kProjCols * 2;
+    pbar = off; off += 8 * 8;
     xproj = off; off += proj_stages * B * kProjRows * 2;
     flag = off; off += 16;
     total = off;
@@ -142,7 +146,10 @@ __device__ __forceinline__ const T* col_source(const DecodeParams& p, int col, i
 // products with one fp32 rounding per step), rounded once to T.
 template <typename T, typename C, int D>
 __device__ void project_columns(const DecodeParams& p, int c_begin, int c_end, uint8_t* smem,
-                                const DecodeSmem& L, int ctid) {
+                                const DecodeSmem& L, int ctid, const CUtensorMap* mq,
+                                const CUtensorMap* mk, const CUtensorMap* mv, uint32_t& gdone,
+                                volatile int* abort_flag) {
+  uint64_t* pbar = reinterpret_cast<uint64_t*>(smem + L.pbar);
   T* wbuf = reinterpret_cast<T*>(smem + L.wproj);   // [S][kProjRows][kProjCols]
   T* xbuf = reinterpret_cast<T*>(smem + L.xproj);   // [S][B][kProjRows]
   const int S = L.proj_stages;
@@ -161,6 +168,16 @@ __device__ void project_columns(const DecodeParams& p, int c_begin, int c_end, u
       const int b0 = active ? (gi / npairs) * 2 : 0;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 
+      // A pass over one whole 64-column block of one weight matrix takes its
+      // weight chunks by TMA (one 128 x 64 box each, off the load/store path
+      // the producers' host requests use); narrower passes use cp.async.
+      // TMA passes number their chunks with a running count g0 + c, which
+      // picks the stage and its barrier's phase.
+      int tw_which = 0, tw_local = 0;
+      (void)col_source<T, D>(p, cb, tw_which, tw_local);
+      const bool tma = ncols == kProjCols && (tw_local % kProjCols) == 0;
+      const CUtensorMap* tmap = tw_which == 0 ? mq : (tw_which == 1 ? mk : mv);
+      const uint32_t g0 = tma ? gdone : 0u;
       auto issue = [&](int chunk, int buf) {
         if (chunk >= nchunks) {  // keep one (empty) group per chunk slot
           cp_async_commit();
@@ -170,6 +187,13 @@ __device__ void project_columns(const DecodeParams& p, int c_begin, int c_end, u
         const int rows = min(kProjRows, H - j0);
         const int pieces_per_row = ncols / 8;
         T* wdst = wbuf + buf * kProjRows * kProjCols;
+        if (tma) {
+          if (ctid == 0) {
+            tc::fence_proxy_async_smem();
+            tc::mbar_expect_tx(&pbar[buf], kProjRows * kProjCols * 2);
+            tc::tma_load_2d(wdst, tmap, tw_local, j0, &pbar[buf]);
+          }
+        } else
         for (int i = ctid; i < rows * pieces_per_row; i += kConsumers) {
           const int r = i / pieces_per_row, pc = i % pieces_per_row;
           int which, local;
@@ -186,18 +210,22 @@ __device__ void project_columns(const DecodeParams& p, int c_begin, int c_end, u
         cp_async_commit();
       };
 
-      for (int c = 0; c < S - 1; ++c) issue(c, c);
+      for (int c = 0; c < S - 1; ++c) issue(c, (g0 + c) % S);
       for (int c = 0; c < nchunks; ++c) {
         // chunk c + S - 1 goes into the slot chunk c - 1 used (every thread
         // passed the barrier after reading it); chunk c is then complete once
         // at most S - 1 newer groups are pending
-        issue(c + S - 1, (c + S - 1) % S);
+        issue(c + S - 1, (g0 + c + S - 1) % S);
         cp_async_wait_stages(S - 1);
+        if (tma && !mbar_wait_bounded(&pbar[(g0 + c) % S], ((g0 + c) / S) & 1, abort_flag)) {
+          if (!*abort_flag) record_timeout(p.status, kSiteFull);
+          *abort_flag = 1;
+        }
         named_bar_sync(kBarConsumers, kConsumers);
         if (active) {
           const int rows = min(kProjRows, H - c * kProjRows);
-          const T* wsrc = wbuf + (c % S) * kProjRows * kProjCols;
-          const T* xs = xbuf + (c % S) * B * kProjRows;
+          const T* wsrc = wbuf + ((g0 + c) % S) * kProjRows * kProjCols;
+          const T* xs = xbuf + ((g0 + c) % S) * B * kProjRows;
           const bool two = b0 + 1 < B;
           // 8 rows per step (rows is a multiple of 16): all loads of a step
           // are issued before its FMA chains, which stay in row order
@@ -230,6 +258,7 @@ __device__ void project_columns(const DecodeParams& p, int c_begin, int c_end, u
         }
         named_bar_sync(kBarConsumers, kConsumers);
       }
+      if (tma) gdone += nchunks;
       if (active) {
         const int col = cb + pair * 2;
         int which, local;
@@ -273,7 +302,9 @@ __device__ __forceinline__ UnitRange unit_range(const DecodeParams& p, int u) {
 }
 
 template <typename T, typename C, int D, int G>
-__global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(
+    const __grid_constant__ CUtensorMap map_wq, const __grid_constant__ CUtensorMap map_wk,
+    const __grid_constant__ CUtensorMap map_wv, const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int EB = KVE<T, C>::EB;
   constexpr int RB = D * EB;   // bytes per cache row
@@ -292,8 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
       mbar_init(&empty[s], kConsumerWarps);
     }
     *abort_flag = 0;
+    uint64_t* pb = reinterpret_cast<uint64_t*>(smem + L.pbar);
+    for (int s = 0; s < 8; ++s) mbar_init(&pb[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  uint32_t gdone = 0;
 
   const int nunits = p.B * p.Hkv * p.splits;
   constexpr int CPR = RB / 16;  // 16-byte chunks per row
@@ -359,13 +394,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeP
     if (2 * nwide >= (int)gridDim.x) {
       for (int bi = blockIdx.x; bi < nwide; bi += gridDim.x)
         project_columns<T, C, D>(p, bi * kProjCols, min(ncol, (bi + 1) * kProjCols), smem, L,
-                                 ctid);
+                                 ctid, &map_wq, &map_wk, &map_wv, gdone, abort_flag);
     } else {
       const int nblk = ncol / 8;
       const int per = nblk / gridDim.x, rem = nblk % gridDim.x;
       const int b0 = blockIdx.x * per + min((int)blockIdx.x, rem);
       const int b1 = b0 + per + ((int)blockIdx.x < rem ? 1 : 0);
-      if (b1 > b0) project_columns<T, C, D>(p, b0 * 8, b1 * 8, smem, L, ctid);
+      if (b1 > b0)
+        project_columns<T, C, D>(p, b0 * 8, b1 * 8, smem, L, ctid, &map_wq, &map_wk, &map_wv,
+                                 gdone, abort_flag);
     }
   }
   if (p.mode == kDecodeProjectOnly) return;  // the producers returned at once
@@ -588,6 +625,12 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, int smem, cudaStrea
   auto kern = decode_fused_kernel<T, C, D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  CUtensorMap mq, mk, mv;
+  const int dt = std::is_same<T, __nv_bfloat16>::value ? DKV_BF16 : DKV_FP16;
+  if (!make_tmap_2d_plain(&mq, p.wq, dt, p.H, (uint64_t)p.Hq * D, kProjCols, kProjRows) ||
+      !make_tmap_2d_plain(&mk, p.wk, dt, p.H, (uint64_t)p.Hkv * D, kProjCols, kProjRows) ||
+      !make_tmap_2d_plain(&mv, p.wv, dt, p.H, (uint64_t)p.Hkv * D, kProjCols, kProjRows))
+    return cudaErrorInvalidValue;
   timer.before(s);
   if (p.len_dev) {
     // the form a stream capture records as a cooperative graph node
@@ -601,9 +644,9 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, int smem, cudaStrea
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, p);
+    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p);
   } else {
-    void* args[] = {const_cast<DecodeParams*>(&p)};
+    void* args[] = {&mq, &mk, &mv, const_cast<DecodeParams*>(&p)};
     e = cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(kThreads), args,
                                     (size_t)smem, s);
   }

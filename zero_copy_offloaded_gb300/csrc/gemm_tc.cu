@@ -175,6 +175,23 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, int dtype, uint64_t rows, 
   return r == CUDA_SUCCESS;
 }
 
+// The same without swizzle: a box lands as box_rows dense rows of box_cols * 2
+// bytes (the decode projection's 64-column weight chunks).
+bool make_tmap_2d_plain(CUtensorMap* map, const void* base, int dtype, uint64_t rows,
+                        uint64_t cols, uint32_t box_cols, uint32_t box_rows) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dtype == DKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Q as [tokens][Hq][D] (row-major [tokens, Hq*D]); box = 64 of D x G heads x
 // TQ tokens, so a box lands as G*TQ rows of 128 bytes, ordered (token, head).
 bool make_tmap_q(CUtensorMap* map, const void* q, int dtype, int D, int Hq, uint64_t tokens,
