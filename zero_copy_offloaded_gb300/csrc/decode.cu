@@ -175,7 +175,7 @@ __device__ void project_columns(const DecodeParams& p, int c_begin, int c_end, u
       // picks the stage and its barrier's phase.
       int tw_which = 0, tw_local = 0;
       (void)col_source<T, D>(p, cb, tw_which, tw_local);
-      const bool tma = ncols == kProjCols && (tw_local % kProjCols) == 0;
+      const bool tma = p.proj_tma && ncols == kProjCols && (tw_local % kProjCols) == 0;
       const CUtensorMap* tmap = tw_which == 0 ? mq : (tw_which == 1 ? mk : mv);
       const uint32_t g0 = tma ? gdone : 0u;
       auto issue = [&](int chunk, int buf) {
@@ -625,11 +625,20 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, int smem, cudaStrea
   auto kern = decode_fused_kernel<T, C, D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  // tensor maps for the projection's weight chunks, only where phase A hands
+  // out whole 64-column blocks (the kernel makes the same choice)
   CUtensorMap mq, mk, mv;
+  memset(&mq, 0, sizeof mq);
+  memset(&mk, 0, sizeof mk);
+  memset(&mv, 0, sizeof mv);
+  DecodeParams pl = p;
+  const int ncol = (p.Hq + 2 * p.Hkv) * D;
+  pl.proj_tma = 2 * ((ncol + kProjCols - 1) / kProjCols) >= grid;
   const int dt = std::is_same<T, __nv_bfloat16>::value ? DKV_BF16 : DKV_FP16;
-  if (!make_tmap_2d_plain(&mq, p.wq, dt, p.H, (uint64_t)p.Hq * D, kProjCols, kProjRows) ||
-      !make_tmap_2d_plain(&mk, p.wk, dt, p.H, (uint64_t)p.Hkv * D, kProjCols, kProjRows) ||
-      !make_tmap_2d_plain(&mv, p.wv, dt, p.H, (uint64_t)p.Hkv * D, kProjCols, kProjRows))
+  if (pl.proj_tma &&
+      (!make_tmap_2d_plain(&mq, p.wq, dt, p.H, (uint64_t)p.Hq * D, kProjCols, kProjRows) ||
+       !make_tmap_2d_plain(&mk, p.wk, dt, p.H, (uint64_t)p.Hkv * D, kProjCols, kProjRows) ||
+       !make_tmap_2d_plain(&mv, p.wv, dt, p.H, (uint64_t)p.Hkv * D, kProjCols, kProjRows)))
     return cudaErrorInvalidValue;
   timer.before(s);
   if (p.len_dev) {
@@ -644,9 +653,9 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, int smem, cudaStrea
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p);
+    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, pl);
   } else {
-    void* args[] = {&mq, &mk, &mv, const_cast<DecodeParams*>(&p)};
+    void* args[] = {&mq, &mk, &mv, &pl};
     e = cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(kThreads), args,
                                     (size_t)smem, s);
   }

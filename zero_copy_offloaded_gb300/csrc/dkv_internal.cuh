@@ -235,6 +235,7 @@ struct DecodeParams {
   CacheLayout lay;     // rows of k_read / v_read / k_host / v_host
   int mode;            // DecodeMode
   int kv_fp8;          // caches hold 8-bit E4M3 (bf16 activations)
+  int proj_tma;       // phase A takes whole 64-column weight blocks by TMA (maps encoded)
   // lengths: len_dev (device, [B]) when set, so that a captured graph replays
   // with the lengths of the step it runs; else the by-value copy below
   const int* len_dev;
