@@ -12,13 +12,16 @@
 //   Phase A  every CTA projects a slice of the [Wq | Wk | Wv] columns for all
 //            sequences (fp32 FMA chain over H in order, rounded once), writes
 //            q and the fresh k/v to a small HBM workspace and appends k/v to
-//            the host cache.  Meanwhile the producer warps already stream the
-//            CTA's first host tiles into the shared-memory ring.
+//            the host cache.  Whole 64-column weight blocks arrive by TMA, so
+//            this HBM traffic stays off the load/store path of the host
+//            requests.  Meanwhile the producer warps already stream the CTA's
+//            first host tiles into the shared-memory ring.
 //   barrier  bounded grid-wide arrival counter (co-residency is guaranteed by
 //            the cooperative launch).
 //   Phase B  units (sequence b, KV head, key-range split) in a static
 //            round-robin.  Producer warps copy host K/V tiles with 16-byte
-//            cp.async into an m-stage ring (mbarrier hand-off); consumer warps
+//            cp.async into an m-stage ring (mbarrier hand-off), one tile in
+//            flight per producer thread; consumer warps
 //            compute the G heads' scores, the online softmax and P.V in fp32
 //            and write one normalised partial (o, lse) per unit.
 // The combine kernel merges the splits with a log-sum-exp weighting.
