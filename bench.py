@@ -345,19 +345,29 @@ class Clocks:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.f.flush()
-        rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r.strip()]
+        lines = open(self.f.name).read().strip().splitlines()
         os.unlink(self.f.name)
+        return self.summarize(lines)
+
+    @staticmethod
+    def summarize(lines):
+        """Median SM clock, max clock and the throttle reasons seen active in
+        `nvidia-smi --format=csv,noheader,nounits` lines of the query Q."""
+        rows = [r.split(",") for r in lines if r.strip()]
         sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
-            try:
-                sm.append(float(r[1]))
-                mx = max(mx, float(r[2]))
-                for n, v in zip(names, r[5:9]):
-                    if v.strip().lower() == "active":
-                        reasons.add(n)
-            except (ValueError, IndexError):  # a partial or non-numeric line
+            if len(r) < 9:  # a partial line (the sampler stopped mid-write)
                 continue
+            try:
+                clk, top = float(r[1]), float(r[2])
+            except ValueError:  # a non-numeric sample
+                continue
+            sm.append(clk)
+            mx = max(mx, top)
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
