@@ -212,13 +212,6 @@ def sweep(args, dkv, torch, dev, stream, flush, pk):
     hbm = pk.get("hbm_gbs") or 6800.0
     print(json.dumps({"sweep": "link", "zero_copy_read_gbs": link_rd,
                       "zero_copy_write_gbs": link_wr}), flush=True)
-    # the fp64 oracle on the tiny decode workload, on every core and on one
-    tw = wl.WORKLOADS["tiny_decode"]
-    oracle_decode_sample(tw)  # builds / loads the oracle outside the timing
-    t_all, cores = min(oracle_decode_sample(tw) for _ in range(3))
-    t_one, _ = min(oracle_decode_sample(tw, threads=1) for _ in range(3))
-    print(json.dumps({"sweep": "oracle_tiny_decode", "kind": "oracle", "tok_s_all_cores": 1 / t_all,
-                      "cores": cores, "tok_s_one_core": 1 / t_one}), flush=True)
     for name, w in wl.WORKLOADS.items():
         if w.phase != "decode":
             continue
@@ -633,6 +626,11 @@ def main():
         dt, cores = oracle_decode_sample(w, 1)
         cpu = {"value": 1.0 / dt, "unit": "tok/s", "cores": cores, "kind": "oracle",
                "sample": f"1 of {w.B} sequences (all {w.Hq} heads, P={w.P}), one step"}
+        # beside it, the same oracle on the tiny decode workload on every core and on one
+        tw = wl.WORKLOADS["tiny_decode"]
+        t_all, _ = min(oracle_decode_sample(tw) for _ in range(3))
+        t_one, _ = min(oracle_decode_sample(tw, threads=1) for _ in range(3))
+        cpu["tiny_decode"] = {"tok_s_all_cores": 1.0 / t_all, "tok_s_one_core": 1.0 / t_one}
 
     if rank == 0:
         line = {
