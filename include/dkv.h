@@ -251,7 +251,9 @@ dkv_status dkv_prefill_layer(dkv_cache* cache, int layer, const void* x, int T, 
 
 /* Synchronise the stream, then return and clear the device status word that
  * bounded waits write (DKV_ERR_TIMEOUT), or DKV_ERR_CUDA if the stream
- * reported an error. */
+ * reported an error.  The word stays set until this call reads it: the
+ * combine kernels of every decode or prefill enqueued while it is set write
+ * NaN outputs instead of merging partials that were never written. */
 dkv_status dkv_sync_status(dkv_cache* cache, void* stream);
 
 /* Tuning overrides for ablations; 0 keeps the adaptor's choice.
@@ -264,8 +266,8 @@ dkv_status dkv_cache_set_tuning(dkv_cache* cache, int splits, int tile_n, int st
  * warps of every dkv_decode on this cache never signal their first host tile,
  * so the consumers' bounded wait expires after about one second; the kernel
  * drains its own copies and returns, and dkv_sync_status reports
- * DKV_ERR_TIMEOUT.  The output of such a call is undefined; the cache rows
- * before the append are untouched and the context stays usable. */
+ * DKV_ERR_TIMEOUT.  The output of such a call is NaN; the cache rows before
+ * the append are untouched and the context stays usable. */
 dkv_status dkv_cache_debug_withhold(dkv_cache* cache, int enable);
 
 const char* dkv_status_str(dkv_status s);
@@ -367,13 +369,31 @@ dkv_status dkv_cache_last_kernel_ms(dkv_cache* cache, float* ms);
  * other threads) race and must be serialised by the caller.  The first call
  * on each device looks up the array's device address (cudaGetSymbolAddress)
  * with that device current; make that first call before any stream capture.
- * Device-side wait timeouts are recorded in the scratch status word only.
+ * The address is looked up again on every call (the lookup allocates
+ * nothing), so a context that was reset and recreated is served correctly.
+ * A device-side wait that gives up (DKV_ERR_TIMEOUT) is recorded in the
+ * scratch status word, which every call clears first, and makes the call's
+ * outputs NaN; dkv_decode_noalloc_status reads it.
  * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY, CUDA, before anything is
  * enqueued. */
 dkv_status dkv_decode_noalloc(const void* x, const void* wq, const void* wk, const void* wv,
                               void* k_cache, void* v_cache, const int32_t* lengths, int batch,
                               int hidden, int n_q_heads, int n_kv_heads, int head_dim,
                               int max_tokens, dkv_dtype dtype, void* out, void* stream);
+
+/* Status of the last dkv_decode_noalloc on the current device, without any
+ * allocation: synchronises `stream`, copies the scratch status word into a
+ * host variable, clears it if set, and returns DKV_OK or the recorded error
+ * (DKV_ERR_TIMEOUT); DKV_ERR_CUDA if the stream reported an error.  Call it
+ * after the dkv_decode_noalloc it should report on and before the next one
+ * (which clears the word). */
+dkv_status dkv_decode_noalloc_status(void* stream);
+
+/* Test hook for the no-allocation path (process-wide): while enabled, the
+ * producers of every dkv_decode_noalloc withhold their first tile's signal so
+ * that the consumers' bounded wait expires after about a second; the call's
+ * outputs are NaN and dkv_decode_noalloc_status reports DKV_ERR_TIMEOUT. */
+dkv_status dkv_decode_noalloc_debug_withhold(int enable);
 
 /* Number of kernel launches the last dkv_decode / dkv_prefill enqueued. */
 int dkv_last_launch_count(void);

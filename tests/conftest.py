@@ -26,3 +26,19 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    # How the appended K/V rows of the tensor-core projections compared with
+    # the oracle's fp32-sequential chain over the whole session.
+    try:
+        from tests.helpers import PROJECTION_TALLY as t
+    except Exception:  # pragma: no cover
+        return
+    if t["elements"]:
+        n = t["elements"]
+        terminalreporter.write_line(
+            f"projection appends vs oracle: {n} elements, bit-exact {t['bit_exact'] / n:.5f}, "
+            f"within 1 ulp {t['within_1ulp'] / n:.6f}, accepted only through the fp32 "
+            f"summation bound {t['fp32_bound_only']} (all near-cancellations; largest "
+            f"|sum| / sum|x w| among them {t['max_cancellation_ratio']:.3g})")

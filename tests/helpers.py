@@ -41,23 +41,60 @@ def ulp_distance(a: np.ndarray, b: np.ndarray) -> np.ndarray:
     return np.abs(ordered(a) - ordered(b))
 
 
+# Tally of every projection comparison in this session (printed by conftest's
+# terminal summary): elements, bit-exact, within 1 ulp, and those accepted
+# only through the fp32 summation bound.
+PROJECTION_TALLY = {"elements": 0, "bit_exact": 0, "within_1ulp": 0, "fp32_bound_only": 0,
+                    "max_cancellation_ratio": 0.0}
+
+
+def storage_ulp(v: np.ndarray, dtype) -> np.ndarray:
+    """Spacing of the 16-bit storage format at |v| (subnormal spacing below the
+    smallest normal)."""
+    p, emin = (8, -126) if dtype == "bf16" else (11, -14)
+    e = np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** emin)))
+    return 2.0 ** (e - (p - 1))
+
+
 def assert_projection_close(got_bits, x_bits, w_bits, dtype, what=""):
     """A tensor-core projection against the oracle's fp32-sequential one.
 
     got_bits [rows, N], x_bits [rows, K], w_bits [K, N].  Each element is
-    within 1 ulp of the oracle's, or (where the sum nearly cancels) within the
-    fp32 summation error bound K * 2^-24 * sum|x_j w_j| plus half an ulp of
-    the exact sum.  Returns (bit-exact fraction, within-1-ulp fraction)."""
+    within 1 ulp of the oracle's, or within the fp32 summation error bound
+    K * 2^-24 * sum|x_j w_j| (plus half an ulp) of the exact sum.  The second
+    case is allowed only where the sum nearly cancels: any two fp32 sums of
+    the same products lie within that bound of the exact sum, so their
+    roundings can be more than 1 ulp apart only if the bound reaches a
+    quarter of the storage ulp at the exact sum, i.e. |exact| is small next
+    to sum|x_j w_j|.  Every element accepted that way is checked to be such a
+    near-cancellation and counted.  Returns (bit-exact fraction, within-1-ulp
+    fraction, number accepted only through the bound)."""
     import oracle
     ref, exact = oracle.project(x_bits, w_bits, dtype, exact=True)
     xf, wf = oracle.decode_bits(x_bits, dtype), oracle.decode_bits(w_bits, dtype)
-    bound = x_bits.shape[1] * 2.0 ** -24 * (np.abs(xf) @ np.abs(wf))
+    mag = np.abs(xf) @ np.abs(wf)
+    bound = x_bits.shape[1] * 2.0 ** -24 * mag
     d = ulp_distance(got_bits, ref)
     g = oracle.decode_bits(got_bits, dtype)
     half_ulp = np.abs(g) * (2.0 ** -8 if dtype == "bf16" else 2.0 ** -11) + 1e-30
-    ok = (d <= 1) | (np.abs(g - exact) <= bound + half_ulp)
+    near = d <= 1
+    in_bound = np.abs(g - exact) <= bound + half_ulp
+    ok = near | in_bound
     assert ok.all(), f"{what}: {(~ok).sum()} elements beyond 1 ulp and the fp32 error bound"
-    return float(np.mean(d == 0)), float(np.mean(d <= 1))
+    fallback = ~near
+    if fallback.any():
+        cancels = bound[fallback] >= storage_ulp(exact[fallback], dtype) / 4
+        assert cancels.all(), (
+            f"{what}: {(~cancels).sum()} elements beyond 1 ulp where the sum does not cancel")
+        ratio = float(np.max(np.abs(exact[fallback]) / np.maximum(mag[fallback], 1e-300)))
+        PROJECTION_TALLY["max_cancellation_ratio"] = max(
+            PROJECTION_TALLY["max_cancellation_ratio"], ratio)
+    n_fb = int(fallback.sum())
+    PROJECTION_TALLY["elements"] += int(d.size)
+    PROJECTION_TALLY["bit_exact"] += int((d == 0).sum())
+    PROJECTION_TALLY["within_1ulp"] += int(near.sum())
+    PROJECTION_TALLY["fp32_bound_only"] += n_fb
+    return float(np.mean(d == 0)), float(np.mean(near)), n_fb
 
 
 def errors(got: np.ndarray, ref: np.ndarray):

@@ -23,6 +23,9 @@ def test_withheld_tile_times_out_then_recovers():
         with pytest.raises(dkv.DkvError) as ei:
             case.cache.sync()
         assert ei.value.name == "DKV_ERR_TIMEOUT"
+        # the combine saw the error: NaN outputs, not a merge of unwritten partials
+        import torch
+        assert torch.isnan(out.float()).all()
         # the status word was cleared by the read; the prefix is intact
         assert np.array_equal(case.cache.k_host[:, :, : w.P], case.k0[:, :, : w.P])
         dkv.dkv_cache_debug_withhold(case.cache.h, False)

@@ -26,7 +26,8 @@ __all__ = [
     "dkv_cache_last_kernel_ms", "dkv_cache_alloc_paged", "dkv_cache_set_page_table",
     "PagedKVCache", "LayeredKVCache", "dkv_cache_alloc_layered", "dkv_decode_layer",
     "dkv_prefill_layer", "dkv_step_graph_capture", "dkv_step_graph_launch",
-    "dkv_cache_alloc_ex", "KV_FORMATS",
+    "dkv_cache_alloc_ex", "KV_FORMATS", "dkv_decode_noalloc", "dkv_decode_noalloc_status",
+    "dkv_decode_noalloc_debug_withhold",
 ]
 
 BF16 = 0
@@ -119,6 +120,8 @@ def lib(build_if_missing: bool = False):
         "dkv_cache_kernel_timing": [P, I],
         "dkv_cache_last_kernel_ms": [P, ctypes.POINTER(ctypes.c_float)],
         "dkv_decode_noalloc": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P],
+        "dkv_decode_noalloc_status": [P],
+        "dkv_decode_noalloc_debug_withhold": [I],
         "dkv_project": [P, P, P, I, I, I, I, P],
         "dkv_cache_debug_withhold": [P, I],
     }
@@ -349,11 +352,23 @@ def dkv_prefill_staged(h, x, T, wq, wk, wv, hidden, n_q_heads, out, k_stage, v_s
 def dkv_decode_noalloc(x, wq, wk, wv, k_cache, v_cache, lengths, batch, hidden, n_q_heads,
                        n_kv_heads, head_dim, max_tokens, dtype, out, stream=None):
     """dkv_decode on caller-owned buffers with no allocation (see include/dkv.h)."""
-    lens = np.ascontiguousarray(lengths, dtype=np.int32)
+    lens = np.ascontiguousarray(lengths, dtype=np.int32).reshape(-1)
+    if lens.size < batch:
+        raise ValueError(f"lengths holds {lens.size} entries for a batch of {batch}")
     _check(lib().dkv_decode_noalloc(_ptr(x), _ptr(wq), _ptr(wk), _ptr(wv), _ptr(k_cache),
                                     _ptr(v_cache), lens.ctypes.data, batch, hidden, n_q_heads,
                                     n_kv_heads, head_dim, max_tokens, _DTYPE[dtype], _ptr(out),
                                     _stream(stream)), "dkv_decode_noalloc")
+
+
+def dkv_decode_noalloc_status(stream=None):
+    """Status of the last dkv_decode_noalloc on the current device (raises on an error)."""
+    _check(lib().dkv_decode_noalloc_status(_stream(stream)), "dkv_decode_noalloc_status")
+
+
+def dkv_decode_noalloc_debug_withhold(enable=True):
+    _check(lib().dkv_decode_noalloc_debug_withhold(int(bool(enable))),
+           "dkv_decode_noalloc_debug_withhold")
 
 
 class KVCache:

@@ -602,11 +602,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(
 }
 
 // Split-KV combine: o = sum_i 2^(lse_i - M) o_i / sum_i 2^(lse_i - M).
+// If a device-side wait of the fused kernel gave up (the status word holds an
+// error), some partials were never written: the outputs are NaN instead of a
+// merge of stale scratch.
 template <typename T>
 __global__ void decode_combine_kernel(const float* __restrict__ part_o,
                                       const float* __restrict__ part_lse, T* __restrict__ out,
                                       int splits, int D, DeviceStatus* status) {
   const int bh = blockIdx.x;
+  if (*(volatile int*)&status->code != 0) {
+    for (int d = threadIdx.x; d < D; d += blockDim.x) out[(size_t)bh * D + d] = DT<T>::from_f(NAN);
+    if (blockIdx.x == 0 && threadIdx.x == 0) status->grid_arrive = 0u;
+    return;
+  }
   const float* lse = part_lse + (size_t)bh * splits;
   float M = -INFINITY;
   for (int i = 0; i < splits; ++i) M = fmaxf(M, lse[i]);

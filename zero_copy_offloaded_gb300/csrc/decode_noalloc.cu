@@ -14,7 +14,6 @@
 
 #include <algorithm>
 #include <cmath>
-#include <mutex>
 
 #include "dkv_internal.cuh"
 
@@ -26,13 +25,13 @@ namespace {
 
 // Maximum scratch this entry point can use: 8 MiB per device.
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
-constexpr int kMaxDevices = 64;
 
 // Shared by every call on a device; keeps the last call's contents.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+// Test hook: when set, the next calls' producers withhold their first tile's
+// signal so that the consumers' bounded wait expires (process-wide).
+int g_debug_withhold = 0;
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
@@ -41,22 +40,19 @@ dkv_status err(dkv_status s, const char* msg) {
   return s;
 }
 
-// Device address of the scratch array on `dev` (which must be current).  The
-// name g_noalloc_scratch in host code is only a host-side stand-in, so the
-// address is looked up once per device with cudaGetSymbolAddress.
-dkv_status scratch_address(int dev, void** out) {
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (dev < 0 || dev >= kMaxDevices) return err(DKV_ERR_UNSUPPORTED, "device index out of range");
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p) {
-      cudaGetLastError();
-      return err(DKV_ERR_CUDA, "cudaGetSymbolAddress of the no-allocation scratch failed");
-    }
-    g_scratch_addr[dev] = p;
+// Device address of the scratch array on the current device.  The name
+// g_noalloc_scratch in host code is only a host-side stand-in, so the address
+// is looked up with cudaGetSymbolAddress; the lookup is repeated on every call
+// (it allocates nothing), so an address never outlives the context it was
+// taken in (after a cudaDeviceReset the module is loaded again elsewhere).
+dkv_status scratch_address(void** out) {
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || !p) {
+    cudaGetLastError();
+    return err(DKV_ERR_CUDA, "cudaGetSymbolAddress of the no-allocation scratch failed");
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return DKV_OK;
 }
 
@@ -93,7 +89,7 @@ extern "C" dkv_status dkv_decode_noalloc(const void* x, const void* wq, const vo
   if (e != cudaSuccess) return err(DKV_ERR_CUDA, "cudaGetDevice failed");
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   void* scratch = nullptr;
-  dkv_status st = scratch_address(dev, &scratch);
+  dkv_status st = scratch_address(&scratch);
   if (st != DKV_OK) return st;
 
   // Same tile and ring as dkv_decode's default choice.
@@ -153,6 +149,7 @@ extern "C" dkv_status dkv_decode_noalloc(const void* x, const void* wq, const vo
   p.lay.S_max = max_tokens;
   p.splits = splits; p.tile_n = N; p.stages = stages;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  p.debug_withhold = g_debug_withhold;
   for (int b = 0; b < kMaxBatch; ++b) p.len[b] = b < batch ? lengths[b] : 0;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -169,5 +166,39 @@ extern "C" dkv_status dkv_decode_noalloc(const void* x, const void* wq, const vo
     cudaGetLastError();
     return err(DKV_ERR_CUDA, cudaGetErrorString(e));
   }
+  return DKV_OK;
+}
+
+// The status of the last dkv_decode_noalloc on this device: waits for
+// `stream`, reads the status word at the head of the scratch array and clears
+// it.  No allocation: the word is copied into a host variable.
+extern "C" dkv_status dkv_decode_noalloc_status(void* stream) {
+  using namespace dkv;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return err(DKV_ERR_CUDA, cudaGetErrorString(e));
+  }
+  DeviceStatus h;
+  e = cudaMemcpyFromSymbol(&h, g_noalloc_scratch, sizeof h, 0, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return err(DKV_ERR_CUDA, "reading the no-allocation status word failed");
+  }
+  if (h.code == 0) return DKV_OK;
+  const DeviceStatus zero = {};
+  e = cudaMemcpyToSymbol(g_noalloc_scratch, &zero, sizeof zero, 0, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return err(DKV_ERR_CUDA, "clearing the no-allocation status word failed");
+  }
+  char msg[96];
+  snprintf(msg, sizeof msg, "a device-side wait gave up (site %d)", h.site);
+  return err(static_cast<dkv_status>(h.code), msg);
+}
+
+extern "C" dkv_status dkv_decode_noalloc_debug_withhold(int enable) {
+  g_debug_withhold = enable ? 1 : 0;
   return DKV_OK;
 }

@@ -644,12 +644,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // over the chunks c = 0 .. (len+t)/C that row sees, in one pass with a running
 // max (what is accumulated is rescaled when a chunk's lse exceeds it).  D/16
 // threads per row, each owning 16 consecutive outputs: two 16-byte loads of
-// the fp16 partials per chunk (32 contiguous bytes per thread).
+// the fp16 partials per chunk (32 contiguous bytes per thread).  If a wait of
+// the fused kernel gave up (the status word holds an error), the outputs are
+// NaN rather than a merge of partials that were never written.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) prefill_combine_tc_kernel(
     const __half* __restrict__ part_o, const float* __restrict__ part_lse,
     const int* __restrict__ part_k, T* __restrict__ out, LenArray len, int B, int T_, int Hq,
-    int Hkv) {
+    int Hkv, const DeviceStatus* status) {
   constexpr int TPR = D / 16;           // threads per row
   constexpr int RPB = 128 / TPR;        // rows per block
   const size_t R = (size_t)B * T_ * Hq;
@@ -665,6 +667,17 @@ __global__ void __launch_bounds__(128) prefill_combine_tc_kernel(
   // partial row of (b, t, h) inside each chunk's R rows: block (b, kvh), row (t, g)
   const size_t pr = (size_t)kh * T_ * G + (size_t)t * G + h % G;
   const int last = (len.v[b] + t) / kC;
+  if (*(const volatile int*)&status->code != 0) {
+    if (active) {
+      uint32_t r[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(NAN);
+      uint4* dst = reinterpret_cast<uint4*>(out + row * D) + 2 * sub;
+      dst[0] = pack8<T>(r, 1.f);
+      dst[1] = pack8<T>(r + 8, 1.f);
+    }
+    return;
+  }
   float M = -INFINITY;
   float acc[16];
 #pragma unroll
@@ -727,7 +740,7 @@ cudaError_t launch_t(const TcArgs& args, const CUtensorMap& mq, const CUtensorMa
   constexpr int RPB = 128 / (D / 16);
   prefill_combine_tc_kernel<T, D><<<(unsigned)((R + RPB - 1) / RPB), 128, 0, s>>>(
       static_cast<const __half*>(args.part_o), args.part_lse, args.part_k, static_cast<T*>(out),
-      len, args.B, args.T, args.Hq, args.Hkv);
+      len, args.B, args.T, args.Hq, args.Hkv, args.status);
   return cudaGetLastError();
 }
 

@@ -164,14 +164,21 @@ def fill_cache(w: Workload, k_out: np.ndarray, v_out: np.ndarray, s_max: int | N
     Each (b, kv head) slice draws from its own sub-stream, so slices can be
     regenerated independently.
     """
+    import concurrent.futures as cf
+    import os
     s_max = s_max or w.S_max
     k4 = k_out.reshape(w.B, w.Hkv, s_max, w.D)
     v4 = v_out.reshape(w.B, w.Hkv, s_max, w.D)
-    for b in range(w.B):
-        for h in range(w.Hkv):
-            kk, vv = cache_slice(w, b, h)
-            k4[b, h, : w.P] = kk
-            v4[b, h, : w.P] = vv
+
+    def one(bh):
+        b, h = divmod(bh, w.Hkv)
+        kk, vv = cache_slice(w, b, h)
+        k4[b, h, : w.P] = kk
+        v4[b, h, : w.P] = vv
+    # the slices are independent streams: draw them on several threads
+    n = w.B * w.Hkv
+    with cf.ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1, n))) as ex:
+        list(ex.map(one, range(n)))
 
 
 def cache_slice(w: Workload, b: int, h: int):
