@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--no-extras", action="store_true",
                     help="only the headline decode (no baselines, prefill, oracle timing)")
     ap.add_argument("--prefill-only", action="store_true")
+    ap.add_argument("--profile-prefill", action="store_true",
+                    help="profiling aid: two warm-up prefill calls, then one fused prefill and "
+                         "one naive untiled prefill of --prefill-workload, untimed")
     ap.add_argument("--sweep", action="store_true",
                     help="one JSON line per workload: every decode workload with its naive and "
                          "copy-to-HBM baselines, then every prefill workload")
@@ -193,6 +196,108 @@ def bench_multilayer(dkv, torch, dev, stream, flush, link_rd, steps, layers=32, 
             "best_ms": best}
 
 
+def _timed_steps(torch, stream, flush, fn, steps, warmup, min_s=0.3, max_steps=2000):
+    """`warmup` untimed calls, then at least `steps` timed ones (CUDA events
+    on the launching stream, L2 flushed outside the events), continued until
+    `min_s` of wall time has passed so that the clock sampler sees the region."""
+    for _ in range(max(warmup, 3)):
+        flush.zero_()
+        fn()
+    ms = []
+    t0 = time.perf_counter()
+    while len(ms) < steps or (time.perf_counter() - t0 < min_s and len(ms) < max_steps):
+        ms.append(_time_once(torch, stream, flush, fn))
+    return ms
+
+
+def bench_decode_config(w, dkv, torch, dev, stream, flush, link_rd, steps, warmup, clock_index,
+                        baselines=True):
+    """One decode workload on its own cache: median step time, the fused
+    kernel's time and host-link rate against the link probe, the SM clock
+    sampled during the timed steps, and (baselines) the naive untiled
+    zero-copy attention, copy-to-HBM-then-attend and separate-kernel times on
+    the same cache."""
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+    cache = dkv.KVCache(w.B, w.Hkv, w.D, w.S_max, w.dtype)
+    wl.fill_cache(w, cache.k_host, cache.v_host)
+    dense = wl.make_dense(w)
+    x, wq, wk, wv = (torch.from_numpy(dense[k].view(np.int16)).view(tdt).to(dev)
+                     for k in ("x", "wq", "wk", "wv"))
+    x = x.reshape(w.B, 1, w.H)
+    out = torch.empty((w.B, 1, w.Hq, w.D), dtype=tdt, device=dev)
+    lens = np.full(w.B, w.P, np.int32)
+    dkv.dkv_cache_reserve(cache.h, w.Hq, 1)
+    dkv.dkv_cache_kernel_timing(cache.h, True)
+    kern = []
+
+    def step():
+        cache.set_lengths(lens)
+        cache.decode(x, wq, wk, wv, w.Hq, out, stream)
+        kern.append(dkv.dkv_cache_last_kernel_ms(cache.h))
+    clocks = Clocks(clock_index)
+    clocks.start()
+    ms = _timed_steps(torch, stream, flush, step, steps, warmup)
+    clk = clocks.stop()
+    kern_ms = statistics.median(kern[max(warmup, 3):])
+    step_ms = statistics.median(ms)
+    hb = w.host_read_bytes()
+    res = {"B": w.B, "P": w.P, "D": w.D, "Hq": w.Hq, "Hkv": w.Hkv, "dtype": w.dtype,
+           "spike_frac": w.spike_frac, "steps_timed": len(ms), "step_ms": step_ms,
+           "tok_s": w.B / (step_ms * 1e-3), "fused_kernel_ms": kern_ms,
+           "host_link_gbs": hb / (kern_ms * 1e-3) / 1e9,
+           "frac_of_link": hb / (kern_ms * 1e-3) / 1e9 / link_rd, "clocks": clk}
+    if baselines:
+        q = torch.randn((w.B, w.Hq, w.D), device=dev).to(tdt)
+        o2 = torch.empty_like(q)
+        cache.set_lengths(lens)
+        res["naive_zero_copy_ms"] = min(
+            _time_once(torch, stream, flush,
+                       lambda: dkv.dkv_attend_naive(cache.h, q, w.Hq, o2, stream))
+            for _ in range(3))
+        cbytes = w.B * w.Hkv * w.S_max * w.D * 2
+        ks = torch.empty(cbytes, dtype=torch.uint8, device=dev)
+        vs = torch.empty(cbytes, dtype=torch.uint8, device=dev)
+
+        def staged():
+            cache.set_lengths(lens)
+            dkv.dkv_decode_staged(cache.h, x, wq, wk, wv, w.H, w.Hq, out, ks, vs, stream)
+        res["copy_to_hbm_then_attend_ms"] = min(_time_once(torch, stream, flush, staged)
+                                                for _ in range(3))
+        del ks, vs
+
+        def unfused():
+            cache.set_lengths(lens)
+            dkv.dkv_decode_unfused(cache.h, x, wq, wk, wv, w.H, w.Hq, out, stream)
+        res["separate_kernels_ms"] = min(_time_once(torch, stream, flush, unfused)
+                                         for _ in range(3))
+    cache.free()
+    return res
+
+
+def bench_configs(args, dkv, torch, dev, stream, flush, pk, link_rd, link_wr, hbm_rd,
+                  clock_index):
+    """Every other workload of the benchmark's configuration list, compactly:
+    the tiny decode, the long-context sweep (batch 1 and 4 at 16K, 64K and 128K
+    cached tokens, 1 % of keys x8) and the fp16 head_dim-64 MHA decode and
+    prefill, each with its baselines and its own clock record."""
+    res = {}
+    for name in ("tiny_decode", "longctx_b1_s16k", "longctx_b1_s64k", "longctx_b1_s128k",
+                 "longctx_b4_s16k", "longctx_b4_s64k", "longctx_b4_s128k", "mha_fp16_decode"):
+        res[name] = bench_decode_config(wl.WORKLOADS[name], dkv, torch, dev, stream, flush,
+                                        link_rd, args.steps, args.warmup, clock_index)
+    a2 = argparse.Namespace(**vars(args))
+    a2.prefill_workload = "mha_fp16_prefill"
+    res["mha_fp16_prefill"] = bench_prefill(a2, dkv, torch, dev, stream, flush, pk, link_rd,
+                                            link_wr, hbm_rd, clock_index=clock_index)
+    # the Llama-3-8B-shaped chunked prefill on an 8-bit E4M3 cache
+    a3 = argparse.Namespace(**vars(args))
+    a3.prefill_workload = "llama8b_prefill"
+    res["llama8b_prefill_e4m3"] = bench_prefill(a3, dkv, torch, dev, stream, flush, pk, link_rd,
+                                                link_wr, hbm_rd, clock_index=clock_index,
+                                                kv_format="e4m3")
+    return res
+
+
 def sweep(args, dkv, torch, dev, stream, flush, pk):
     """All workloads, one JSON line each (secondary measurements, not the headline)."""
     # link denominators over a 1 GiB mapped buffer
@@ -212,57 +317,14 @@ def sweep(args, dkv, torch, dev, stream, flush, pk):
     hbm = pk.get("hbm_gbs") or 6800.0
     print(json.dumps({"sweep": "link", "zero_copy_read_gbs": link_rd,
                       "zero_copy_write_gbs": link_wr}), flush=True)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    clock_index = vis.split(",")[0] if vis else "0"
     for name, w in wl.WORKLOADS.items():
         if w.phase != "decode":
             continue
-        tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
-        cache = dkv.KVCache(w.B, w.Hkv, w.D, w.S_max, w.dtype)
-        wl.fill_cache(w, cache.k_host, cache.v_host)
-        dense = wl.make_dense(w)
-        x, wq, wk, wv = (torch.from_numpy(dense[k].view(np.int16)).view(tdt).to(dev)
-                         for k in ("x", "wq", "wk", "wv"))
-        x = x.reshape(w.B, 1, w.H)
-        out = torch.empty((w.B, 1, w.Hq, w.D), dtype=tdt, device=dev)
-        lens = np.full(w.B, w.P, np.int32)
-        dkv.dkv_cache_kernel_timing(cache.h, True)
-
-        def step():
-            cache.set_lengths(lens)
-            cache.decode(x, wq, wk, wv, w.Hq, out, stream)
-        for _ in range(3):
-            step()
-        ms = [_time_once(torch, stream, flush, step) for _ in range(max(args.steps, 5))]
-        kern = dkv.dkv_cache_last_kernel_ms(cache.h)
-        q = torch.randn((w.B, w.Hq, w.D), device=dev).to(tdt)
-        o2 = torch.empty_like(q)
-        cache.set_lengths(lens)
-        naive = min(_time_once(torch, stream, flush,
-                               lambda: dkv.dkv_attend_naive(cache.h, q, w.Hq, o2, stream))
-                    for _ in range(3))
-        cbytes = w.B * w.Hkv * w.S_max * w.D * 2
-        ks = torch.empty(cbytes, dtype=torch.uint8, device=dev)
-        vs = torch.empty(cbytes, dtype=torch.uint8, device=dev)
-
-        def staged():
-            cache.set_lengths(lens)
-            dkv.dkv_decode_staged(cache.h, x, wq, wk, wv, w.H, w.Hq, out, ks, vs, stream)
-        staged_ms = min(_time_once(torch, stream, flush, staged) for _ in range(3))
-        del ks, vs
-
-        def unfused():
-            cache.set_lengths(lens)
-            dkv.dkv_decode_unfused(cache.h, x, wq, wk, wv, w.H, w.Hq, out, stream)
-        unfused_ms = min(_time_once(torch, stream, flush, unfused) for _ in range(3))
-        cache.free()
-        step_ms = statistics.median(ms)
-        hb = w.host_read_bytes()
-        print(json.dumps({
-            "sweep": name, "phase": "decode", "B": w.B, "P": w.P, "D": w.D, "Hq": w.Hq,
-            "Hkv": w.Hkv, "dtype": w.dtype, "step_ms": step_ms, "tok_s": w.B / (step_ms * 1e-3),
-            "fused_kernel_ms": kern, "host_link_gbs": hb / (kern * 1e-3) / 1e9,
-            "frac_of_link": hb / (kern * 1e-3) / 1e9 / link_rd,
-            "naive_zero_copy_ms": naive, "copy_to_hbm_then_attend_ms": staged_ms,
-            "separate_kernels_ms": unfused_ms}), flush=True)
+        res = bench_decode_config(w, dkv, torch, dev, stream, flush, link_rd, args.steps,
+                                  args.warmup, clock_index)
+        print(json.dumps({"sweep": name, "phase": "decode", **res}), flush=True)
     for name in ("llama8b_decode", "longctx_b1_s128k"):
         res = bench_fp8_decode(wl.WORKLOADS[name], dkv, torch, dev, stream, flush, link_rd,
                                args.steps)
@@ -451,6 +513,24 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     if args.sweep:
         return sweep(args, dkv, torch, dev, stream, flush, pk)
+    if args.profile_prefill:
+        w = wl.WORKLOADS[args.prefill_workload]
+        tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+        cache = dkv.KVCache(w.B, w.Hkv, w.D, w.S_max, w.dtype)
+        wl.fill_cache(w, cache.k_host, cache.v_host)
+        dense = wl.make_dense(w)
+        x, wq, wk, wv = (torch.from_numpy(dense[k].view(np.int16)).view(tdt).to(dev)
+                         for k in ("x", "wq", "wk", "wv"))
+        out = torch.empty((w.B, w.T, w.Hq, w.D), dtype=tdt, device=dev)
+        lens = np.full(w.B, w.P, np.int32)
+        for i in range(3):
+            cache.set_lengths(lens)
+            cache.prefill(x, wq, wk, wv, w.Hq, out, stream)
+        cache.set_lengths(lens)
+        dkv.dkv_prefill_naive(cache.h, x, w.T, wq, wk, wv, w.H, w.Hq, out, stream)
+        cache.sync(stream)
+        cache.free()
+        return
     if args.prefill_only:
         # prefill alone (profiling aid): link/HBM rates from the probes, then the prefill
         probe_cache = dkv.KVCache(1, 8, 128, 65536, "bf16")
@@ -607,8 +687,9 @@ def main():
             "separate_kernels_ms": unfused_ms,
             "hbm_staging_bytes": 2 * cache_bytes,
         }
+        clock_index = vis.split(",")[local] if vis else str(local)
         extras["prefill"] = bench_prefill(args, dkv, torch, dev, stream, flush, pk, link_rd,
-                                          link_wr, hbm_rd)
+                                          link_wr, hbm_rd, clock_index=clock_index)
     cache.free()
     if not args.no_extras:
         # the same decode on a paged cache (16-token pages, shuffled page table)
@@ -620,6 +701,9 @@ def main():
         # a 32-layer step of small per-layer caches: launches per layer vs one graph
         extras["multilayer_decode_step"] = bench_multilayer(dkv, torch, dev, stream, flush,
                                                             link_rd, args.steps)
+        # every other configuration, compactly, each with its baselines and clocks
+        extras["configs"] = bench_configs(args, dkv, torch, dev, stream, flush, pk, link_rd,
+                                          link_wr, hbm_rd, clock_index)
 
     cpu = None
     if rank == 0 and not args.no_extras:
@@ -671,11 +755,31 @@ def _time_once(torch, stream, flush, fn):
     return a.elapsed_time(b)
 
 
-def bench_prefill(args, dkv, torch, dev, stream, flush, pk, link_rd, link_wr, hbm_rd):
+def bench_prefill(args, dkv, torch, dev, stream, flush, pk, link_rd, link_wr, hbm_rd,
+                  clock_index=None, naive_max_ms=400.0, kv_format="native"):
+    """One prefill workload: the whole call (Q projection + fused kernel +
+    combine) timed over `steps` calls after `warmup` (median; lengths reset
+    before each so every call appends at the same position), the fused
+    kernel's own time, the SM clock during the timed calls, TFLOP/s against
+    the min-of-rooflines bound, and two baselines on the same inputs:
+    copy-to-HBM-then-prefill and the naive untiled zero-copy prefill (every
+    (Q tile, chunk) pair fetching its chunk across the link; timed only if one
+    call stays under `naive_max_ms`).  kv_format "e4m3": the same workload on an
+    8-bit E4M3 cache (the values converted with torch's float8 type as input
+    construction), half the host bytes; the baselines are 16-bit only."""
     w = wl.WORKLOADS[args.prefill_workload]
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
-    cache = dkv.KVCache(w.B, w.Hkv, w.D, w.S_max, w.dtype)
-    wl.fill_cache(w, cache.k_host, cache.v_host)
+    fp8 = kv_format == "e4m3"
+    cache = dkv.KVCache(w.B, w.Hkv, w.D, w.S_max, w.dtype, kv_format=kv_format)
+    if fp8:
+        for b in range(w.B):
+            for h in range(w.Hkv):
+                kk, vv = wl.cache_slice(w, b, h)
+                for host, bits in ((cache.k_host, kk), (cache.v_host, vv)):
+                    f = torch.from_numpy(wl.bits_to_f32(bits, w.dtype)).to(torch.float8_e4m3fn)
+                    host[b, h, :w.P] = f.view(torch.uint8).numpy()
+    else:
+        wl.fill_cache(w, cache.k_host, cache.v_host)
     dense = wl.make_dense(w)
     x, wq, wk, wv = (torch.from_numpy(dense[k].view(np.int16)).view(tdt).to(dev)
                      for k in ("x", "wq", "wk", "wv"))
@@ -683,62 +787,79 @@ def bench_prefill(args, dkv, torch, dev, stream, flush, pk, link_rd, link_wr, hb
     lens = np.full(w.B, w.P, np.int32)
     dkv.dkv_cache_reserve(cache.h, w.Hq, w.T)
     dkv.dkv_cache_kernel_timing(cache.h, True)
-    times, kern = [], []
-    for i in range(5):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kern = []
+
+    def call():
         cache.set_lengths(lens)
-        a.record(stream)
         cache.prefill(x, wq, wk, wv, w.Hq, out, stream)
-        b.record(stream)
-        b.synchronize()
-        if i >= 2:
-            times.append(a.elapsed_time(b))
-            kern.append(dkv.dkv_cache_last_kernel_ms(cache.h))
+        kern.append(dkv.dkv_cache_last_kernel_ms(cache.h))
+    clocks = Clocks(clock_index) if clock_index is not None else None
+    if clocks:
+        clocks.start()
+    times = _timed_steps(torch, stream, flush, call, max(args.steps, 10), args.warmup)
+    clk = clocks.stop() if clocks else None
+    kern = kern[max(args.warmup, 3):]
     cache.sync(stream)
-    # baseline: copy the cached prefix to HBM, then the same fused prefill from there
-    nstage = w.B * w.Hkv * w.S_max * w.D
-    k_stage = torch.empty(nstage, dtype=tdt, device=dev)
-    v_stage = torch.empty(nstage, dtype=tdt, device=dev)
-    staged = []
-    for i in range(4):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def naive():
         cache.set_lengths(lens)
-        a.record(stream)
-        dkv.dkv_prefill_staged(cache.h, x, w.T, wq, wk, wv, w.H, w.Hq, out, k_stage, v_stage,
-                               stream)
-        b.record(stream)
-        b.synchronize()
-        if i >= 2:
-            staged.append(a.elapsed_time(b))
-    cache.sync(stream)
-    del k_stage, v_stage
+        dkv.dkv_prefill_naive(cache.h, x, w.T, wq, wk, wv, w.H, w.Hq, out, stream)
+    naive_ms = staged_ms = None
+    nstage = w.B * w.Hkv * w.S_max * w.D
+    if not fp8:
+        naive_ms = _time_once(torch, stream, flush, naive)   # first call: also the size check
+        if naive_ms <= naive_max_ms:
+            naive_ms = min([naive_ms] + [_time_once(torch, stream, flush, naive)
+                                         for _ in range(2)])
+        cache.sync(stream)
+        # baseline: copy the cached prefix to HBM, then the same fused prefill from there
+        k_stage = torch.empty(nstage, dtype=tdt, device=dev)
+        v_stage = torch.empty(nstage, dtype=tdt, device=dev)
+
+        def staged():
+            cache.set_lengths(lens)
+            dkv.dkv_prefill_staged(cache.h, x, w.T, wq, wk, wv, w.H, w.Hq, out, k_stage,
+                                   v_stage, stream)
+        staged_ms = statistics.median(_timed_steps(torch, stream, flush, staged, 5, 2, min_s=0))
+        cache.sync(stream)
+        del k_stage, v_stage
     info = dkv.dkv_cache_info(cache.h)
     cache.free()
-    ms = statistics.mean(times)
-    tr = ncu_traffic(f"prefill_tc_kernel/{w.name}", ["prefill_tc.cu", "dkv_internal.cuh",
-                                                      "tc_common.cuh"])
+    ms = statistics.median(times)
+    tr = None if fp8 else ncu_traffic(f"prefill_tc_kernel/{w.name}",
+                                      ["prefill_tc.cu", "dkv_internal.cuh", "tc_common.cuh"])
     flops = w.flops()
     tflops_peak = pk.get("bf16_tflops") or 1900.0
-    t_link_rd = w.host_read_bytes() / (link_rd * 1e9)
-    t_link_wr = w.host_write_bytes() / (link_wr * 1e9)
+    hb_rd = w.host_read_bytes() // (2 if fp8 else 1)
+    hb_wr = w.host_write_bytes() // (2 if fp8 else 1)
+    t_link_rd = hb_rd / (link_rd * 1e9)
+    t_link_wr = hb_wr / (link_wr * 1e9)
     t_hbm = w.hbm_min_bytes() / (hbm_rd * 1e9)
     t_flop = flops / (tflops_peak * 1e12)
     t_roof = max(t_link_rd, t_link_wr, t_hbm, t_flop)
-    return {"workload": w.name, "ms": ms, "fused_kernel_ms": statistics.mean(kern),
+    dram = (tr["dram_bytes"] + tr["combine_dram_read_bytes"] + tr["combine_dram_write_bytes"]
+            if tr else None)
+    return {"workload": w.name, "kv_format": kv_format, "host_read_bytes": hb_rd,
+            "host_write_bytes": hb_wr, "ms": ms, "calls_timed": len(times),
+            "fused_kernel_ms": statistics.median(kern),
             "tflops": flops / (ms * 1e-3) / 1e12, "flops": flops,
             "roofline_ms": t_roof * 1e3,
             "roofline_terms_ms": {"link_read": t_link_rd * 1e3, "link_write": t_link_wr * 1e3,
                                   "hbm": t_hbm * 1e3, "tensor": t_flop * 1e3},
             "frac_of_roofline": t_roof / (ms * 1e-3),
-            "copy_to_hbm_then_prefill_ms": statistics.mean(staged),
+            "clocks": clk,
+            "copy_to_hbm_then_prefill_ms": staged_ms,
+            "naive_zero_copy_ms": naive_ms if naive_ms and naive_ms <= naive_max_ms else None,
+            "naive_zero_copy_first_call_ms": naive_ms,
             # DRAM bytes of one fused launch and of the combine, from a committed ncu
-            # capture of the current sources (None once they change)
+            # capture of the current sources (None once they change), and the whole
+            # call's DRAM bytes over the algorithmic HBM minimum
             "traffic_dram": tr["dram_bytes"] if tr else None,
             "traffic_dram_combine": (tr["combine_dram_read_bytes"] + tr["combine_dram_write_bytes"]
                                      if tr else None),
-            "hbm_staging_bytes": 2 * nstage * 2,
+            "hbm_min_bytes": w.hbm_min_bytes(),
+            "traffic_dram_over_hbm_min": dram / w.hbm_min_bytes() if dram else None,
+            "hbm_staging_bytes": None if fp8 else 2 * nstage * 2,
             "tensor_peak_tflops": tflops_peak,
             "device_workspace_bytes": info["device_workspace_bytes"]}
 

@@ -337,6 +337,19 @@ dkv_status dkv_prefill_staged(dkv_cache* cache, const void* x, int T, const void
                               const void* wk, const void* wv, int hidden, int n_q_heads,
                               void* out, void* k_stage, void* v_stage, void* stream);
 
+/* Naive untiled zero-copy prefill (measurement baseline for the pages'
+ * CPU-memory-aware tiling, "Paper Notes: DirectKV", Key Ideas (1) and
+ * Experiments & Results, Fig. 12).  Same computation, results and append
+ * as dkv_prefill, from the same fused kernel, but every (Q tile, chunk)
+ * pair gets its own CTA, in the order a Q-stationary kernel streams the
+ * chunks, so each chunk of cached rows crosses the host link once per Q tile
+ * that sees it instead of once.  The outputs are bit-identical to
+ * dkv_prefill's.  Errors as dkv_prefill, plus UNSUPPORTED for a layered or
+ * E4M3 cache. */
+dkv_status dkv_prefill_naive(dkv_cache* cache, const void* x, int T, const void* wq,
+                             const void* wk, const void* wv, int hidden, int n_q_heads,
+                             void* out, void* stream);
+
 /* Kernel timing for measurement: when enabled, each dkv_decode / dkv_prefill
  * records a pair of CUDA events on its stream around its main fused kernel
  * (not the projection or combine launches).  dkv_cache_last_kernel_ms waits

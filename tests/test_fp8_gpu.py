@@ -1,5 +1,5 @@
-"""8-bit E4M3 K/V caches: the fused decode reads half the bytes across the host
-link.  Against the fp64 oracle on the same E4M3 cache: appended K/V rows
+"""8-bit E4M3 K/V caches: the fused decode and prefill read half the bytes
+across the host link.  Against the fp64 oracle on the same E4M3 cache: appended K/V rows
 bit-exact (the same fp32 in-order chain as the oracle, rounded once to E4M3 to
 nearest, ties to even, saturating), outputs max-abs <= 1e-2 and mean-rel <= 2e-3
 (the attention over the decoded E4M3 values; the quantisation of the cache is
@@ -90,8 +90,8 @@ def test_fp8_refusals():
         wq = torch.zeros((64, 256), dtype=torch.bfloat16, device="cuda")
         wk = torch.zeros((64, 128), dtype=torch.bfloat16, device="cuda")
         out = torch.empty((1, 4, 4, 64), dtype=torch.bfloat16, device="cuda")
-        with pytest.raises(dkv.DkvError) as ei:
-            c.prefill(x, wq, wk, wk, 4, out)
+        with pytest.raises(dkv.DkvError) as ei:   # the baselines stay 16-bit only
+            dkv.dkv_prefill_naive(c.h, x, 4, wq, wk, wk, 64, 4, out, None)
         assert ei.value.name == "DKV_ERR_UNSUPPORTED"
         c.set_lengths([3])
         with pytest.raises(dkv.DkvError) as ei:
@@ -104,3 +104,107 @@ def test_fp8_refusals():
     with pytest.raises(dkv.DkvError) as ei:
         dkv.KVCache(1, 2, 64, 64, "fp16", kv_format="e4m3")
     assert ei.value.name == "DKV_ERR_UNSUPPORTED"
+
+
+def e4m3_ulp_distance(a, b):
+    """Distance in representable steps between two arrays of E4M3 codes."""
+    def ordered(x):
+        x = x.astype(np.int32)
+        return np.where(x & 0x80, -(x & 0x7F), x)
+    return np.abs(ordered(a) - ordered(b))
+
+
+def check_prefill_e4m3(case, out, ref, label):
+    """The fused prefill's projection sums on the tensor cores in another
+    order than the oracle's fp32 chain and then rounds once to E4M3.  So each
+    appended code is the oracle's, or one step away where the exact sum lies
+    within the fp32 summation error bound (H * 2^-24 * sum|x_j w_j|) of the
+    midpoint between the two codes.  One E4M3 step is an eighth of the value,
+    so such a code moves outputs by far more than the attention's own error:
+    the outputs are compared with the oracle's attention over the cache as
+    written (the oracle's q, the written K/V rows decoded).  Prefix rows and
+    canaries untouched.  Returns (max-abs beyond rounding, mean-rel, share of
+    appended codes equal to the oracle's)."""
+    import oracle
+    from .helpers import assert_close_beyond_rounding, out_f64
+    w = case.w
+    T = out.shape[1]
+    G = w.Hq // w.Hkv
+    kh, vh = case.k_logical(), case.v_logical()
+    xr = case.dense["x"]
+    exact_n = tot = 0
+    for b in range(w.B):
+        p = int(case.lens[b])
+        for host, new, wm in ((kh, ref["k_new"], case.dense["wk"]),
+                              (vh, ref["v_new"], case.dense["wv"])):
+            g = host[b, :, p:p + T].transpose(1, 0, 2).reshape(T, -1)   # [T, Hkv*D]
+            r = new[b].reshape(T, -1)
+            d = e4m3_ulp_distance(g, r)
+            assert d.max() <= 1, f"{label}: appended code {d.max()} steps from the oracle's"
+            if (d == 1).any():
+                _, ex = oracle.project(xr[b], wm, w.dtype, exact=True)
+                bound = w.H * 2.0 ** -24 * (np.abs(oracle.decode_bits(xr[b], w.dtype))
+                                            @ np.abs(oracle.decode_bits(wm, w.dtype)))
+                mid = (oracle.decode_e4m3(g) + oracle.decode_e4m3(r)) / 2
+                off = d == 1
+                assert np.all(np.abs(ex[off] - mid[off]) <= bound[off]), (
+                    f"{label}: a code one step from the oracle's is not at a rounding tie")
+            exact_n += int((d == 0).sum())
+            tot += d.size
+        assert np.array_equal(kh[b, :, :p], case.k0[b, :, :p])
+        assert np.array_equal(vh[b, :, :p], case.v0[b, :, :p])
+        assert np.all(kh[b, :, p + T:] == case.canary) and np.all(vh[b, :, p + T:] == case.canary)
+    # the oracle's attention over the cache as written
+    att = np.zeros((w.B, T, w.Hq, w.D))
+    for b in range(w.B):
+        p = int(case.lens[b])
+        for kvh in range(w.Hkv):
+            kf = oracle.decode_e4m3(kh[b, kvh, :p + T])
+            vf = oracle.decode_e4m3(vh[b, kvh, :p + T])
+            q = oracle.decode_bits(ref["q"][b, :, kvh * G:(kvh + 1) * G], w.dtype)
+            pos = np.repeat(p + np.arange(T), G)
+            att[b, :, kvh * G:(kvh + 1) * G] = oracle.attend(
+                kf, vf, q.reshape(-1, w.D), pos).reshape(T, G, w.D)
+    got = out_f64(out, w.dtype).reshape(w.B, T, w.Hq, w.D)
+    mx, mr = assert_close_beyond_rounding(got, att, w.dtype, label)
+    return mx, mr, exact_n / tot
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,P,T", [(128, 8, 2, 600, 129), (64, 8, 8, 300, 70),
+                                         (128, 32, 8, 1000, 300), (64, 16, 2, 0, 37)])
+def test_fp8_prefill_shapes(D, Hq, Hkv, P, T):
+    """The KV-stationary prefill on an E4M3 cache: host rows converted in the
+    stationary tile (K to bf16, V to fp16), new rows rounded once to E4M3."""
+    w = wl.Workload("t", "prefill", B=2, H=256, Hq=Hq, Hkv=Hkv, D=D, P=P, T=T,
+                    seed=P + T + D)
+    case = Case(w, lens=[P, P // 2], s_max=P + T + 3, kv_format="e4m3")
+    try:
+        out = case.run_prefill()
+        check_prefill_e4m3(case, out, case.oracle(), f"e4m3 prefill D{D} G{Hq // Hkv} P{P} T{T}")
+        assert list(case.cache.lengths()) == [P + T, P // 2 + T]
+    finally:
+        case.free()
+
+
+def test_fp8_prefill_paged_spiky_then_decode():
+    """Paged E4M3 cache (16-token pages, shuffled), 5 % of the key rows x8, a
+    prefill and then a decode on the grown cache, both against the oracle."""
+    w = wl.Workload("t", "prefill", B=2, H=128, Hq=8, Hkv=2, D=128, P=520, T=90,
+                    spike_frac=0.05, seed=29)
+    case = Case(w, lens=[520, 257], s_max=640, page_tokens=16, kv_format="e4m3")
+    try:
+        out = case.run_prefill()
+        ref = case.oracle()
+        check_prefill_e4m3(case, out, ref, "e4m3 paged prefill")
+        assert case.spare_pages_untouched()
+        # the decode's oracle starts from the cache as the prefill wrote it
+        k_written, v_written = case.k_logical().copy(), case.v_logical().copy()
+        x2 = wl.make_dense(w.with_(T=1, seed=5))["x"]
+        out2 = case.run_decode(to_dev(x2, w.dtype))
+        ref2 = case.oracle(x_bits=x2, k=k_written, v=v_written, lens=case.lens + w.T)
+        from .helpers import assert_close_beyond_rounding, out_f64
+        assert_close_beyond_rounding(out_f64(out2, w.dtype).reshape(w.B, w.Hq, w.D),
+                                     ref2["out"].reshape(w.B, w.Hq, w.D), w.dtype,
+                                     "decode after e4m3 prefill")
+    finally:
+        case.free()

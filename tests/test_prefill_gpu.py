@@ -322,3 +322,31 @@ def test_prefill_bf16_value_chunk_scale():
         check_appends(case, w.T, "V chunk scale")
     finally:
         case.free()
+
+
+@pytest.mark.parametrize("dtype,D,Hq,Hkv,P,T", [("bf16", 128, 8, 2, 600, 129),
+                                               ("fp16", 64, 8, 8, 300, 70)])
+def test_prefill_naive_baseline(dtype, D, Hq, Hkv, P, T):
+    """The naive untiled baseline (one CTA per Q tile and chunk, every pair
+    fetching its chunk from the host): against the oracle, and bit-identical
+    to the fused prefill on the same inputs (the same per-chunk work); the
+    appended rows are written once."""
+    import torch
+    w = wl.Workload("t", "prefill", B=2, H=128, Hq=Hq, Hkv=Hkv, D=D, P=P, T=T, dtype=dtype,
+                    kv_dist="uniform2" if dtype == "fp16" else "normal", seed=P + T + 1)
+    case = Case(w, lens=[P, P // 3], s_max=P + T + 5)
+    try:
+        out_n = case.out_tensor(T)
+        dkv.dkv_prefill_naive(case.cache.h, case.x, T, case.wq, case.wk, case.wv, w.H, w.Hq,
+                              out_n, None)
+        case.cache.sync()
+        ref = case.oracle()
+        check_prefill(case, out_n, ref, f"naive prefill {dtype}")
+        assert list(case.cache.lengths()) == [P + T, P // 3 + T]
+        case.cache.k_host[...] = case.k0
+        case.cache.v_host[...] = case.v0
+        case.cache.set_lengths(case.lens.astype(np.int32))
+        out_f = case.run_prefill()
+        assert torch.equal(out_n.view(torch.int16), out_f.view(torch.int16))
+    finally:
+        case.free()

@@ -22,7 +22,7 @@ __all__ = [
     "dkv_cache_set_lengths", "dkv_cache_get_lengths", "dkv_cache_info", "dkv_cache_reserve",
     "dkv_cache_set_tuning", "dkv_decode", "dkv_prefill", "dkv_sync_status", "dkv_status_str",
     "dkv_last_error", "dkv_probe_read", "dkv_probe_write", "dkv_attend_naive",
-    "dkv_decode_staged", "dkv_prefill_staged", "dkv_decode_unfused", "dkv_last_launch_count", "dkv_cache_kernel_timing",
+    "dkv_decode_staged", "dkv_prefill_staged", "dkv_prefill_naive", "dkv_decode_unfused", "dkv_last_launch_count", "dkv_cache_kernel_timing",
     "dkv_cache_last_kernel_ms", "dkv_cache_alloc_paged", "dkv_cache_set_page_table",
     "PagedKVCache", "LayeredKVCache", "dkv_cache_alloc_layered", "dkv_decode_layer",
     "dkv_prefill_layer", "dkv_step_graph_capture", "dkv_step_graph_launch",
@@ -116,6 +116,7 @@ def lib(build_if_missing: bool = False):
         "dkv_attend_naive": [P, P, I, P, P],
         "dkv_decode_staged": [P, P, P, P, P, I, I, P, P, P, P],
         "dkv_prefill_staged": [P, P, I, P, P, P, I, I, P, P, P, P],
+        "dkv_prefill_naive": [P, P, I, P, P, P, I, I, P, P],
         "dkv_decode_unfused": [P, P, P, P, P, I, I, P, P],
         "dkv_cache_kernel_timing": [P, I],
         "dkv_cache_last_kernel_ms": [P, ctypes.POINTER(ctypes.c_float)],
@@ -347,6 +348,12 @@ def dkv_prefill_staged(h, x, T, wq, wk, wv, hidden, n_q_heads, out, k_stage, v_s
                                     n_q_heads, _ptr(out), _ptr(k_stage), _ptr(v_stage),
                                     _stream(stream)),
            "dkv_prefill_staged")
+
+
+def dkv_prefill_naive(h, x, T, wq, wk, wv, hidden, n_q_heads, out, stream=None):
+    _check(lib().dkv_prefill_naive(h, _ptr(x), T, _ptr(wq), _ptr(wk), _ptr(wv), hidden,
+                                   n_q_heads, _ptr(out), _stream(stream)),
+           "dkv_prefill_naive")
 
 
 def dkv_decode_noalloc(x, wq, wk, wv, k_cache, v_cache, lengths, batch, hidden, n_q_heads,

@@ -1,6 +1,6 @@
 // C ABI of libdkv: the host KV-cache manager, the kernel adaptor and the
 // launch code.  Every compute step runs in the kernels of decode.cu,
-// prefill.cu and probes.cu; this file validates arguments, sizes the
+// prefill_tc.cu, gemm_tc.cu and probes.cu; this file validates arguments, sizes the
 // workspace, picks a precompiled kernel and enqueues it.
 //
 // KV Cache Manager ("Paper Notes: DirectKV", System Architecture): K/V live in
@@ -101,6 +101,7 @@ struct dkv_cache {
 namespace {
 
 bool valid(const dkv_cache* c) { return c != nullptr && c->magic == kMagic; }
+
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -813,7 +814,8 @@ namespace {
 // are appended to the host cache.  Called with the cache's mutex held.
 dkv_status prefill_impl(dkv_cache* c, int layer, const void* x, int T, const void* wq,
                         const void* wk, const void* wv, int hidden, int n_q_heads, void* out,
-                        const void* k_read, const void* v_read, void* stream) {
+                        const void* k_read, const void* v_read, void* stream,
+                        bool naive = false) {
   dkv_status st;
   const int G = n_q_heads / c->Hkv;
   if (!prefill_supported(c->dtype, c->D, G))
@@ -833,7 +835,7 @@ dkv_status prefill_impl(dkv_cache* c, int layer, const void* x, int T, const voi
   PrefillParams p;
   memset(&p, 0, sizeof p);
   p.x = x; p.wk = wk; p.wv = wv; p.q = w;
-  const size_t loff = (size_t)layer * c->layer_elems * 2;  // bytes
+  const size_t loff = (size_t)layer * c->layer_elems * c->kv_eb;  // bytes
   p.k_read = static_cast<const char*>(k_read) + loff;
   p.v_read = static_cast<const char*>(v_read) + loff;
   p.k_host = static_cast<char*>(c->k_dev) + loff;
@@ -847,6 +849,8 @@ dkv_status prefill_impl(dkv_cache* c, int layer, const void* x, int T, const voi
   p.chunk = C; p.nchunks = nchunks;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   p.lay = layout_of(c);
+  p.naive = naive ? 1 : 0;
+  p.kv_fp8 = c->kv_format == DKV_KV_E4M3;
   fill_lens(p.len, c->len);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   g_last_launches = 0;
@@ -873,8 +877,6 @@ dkv_status dkv_prefill_layer(dkv_cache* c, int layer, const void* x, int T, cons
   if (st != DKV_OK) return st;
   if (layer < 0 || layer >= c->layers)
     return fail(DKV_ERR_INVALID_ARG, "layer %d outside [0, %d)", layer, c->layers);
-  if (c->kv_format != DKV_KV_NATIVE)
-    return fail(DKV_ERR_UNSUPPORTED, "prefill needs a 16-bit cache (E4M3 caches serve decode)");
   std::lock_guard<std::mutex> lk(c->mu);
   if ((st = set_device(c)) != DKV_OK) return st;
   return prefill_impl(c, layer, x, T, wq, wk, wv, hidden, n_q_heads, out, c->k_dev, c->v_dev,
@@ -907,6 +909,19 @@ dkv_status dkv_prefill_staged(dkv_cache* c, const void* x, int T, const void* wq
       if (e != cudaSuccess) return cuda_fail(e, "staging cudaMemcpyAsync");
     }
   return prefill_impl(c, 0, x, T, wq, wk, wv, hidden, n_q_heads, out, k_stage, v_stage, stream);
+}
+
+dkv_status dkv_prefill_naive(dkv_cache* c, const void* x, int T, const void* wq,
+                             const void* wk, const void* wv, int hidden, int n_q_heads,
+                             void* out, void* stream) {
+  dkv_status st = check_call(c, x, wq, wk, wv, hidden, n_q_heads, out, T);
+  if (st != DKV_OK) return st;
+  if (c->layers != 1 || c->kv_format != DKV_KV_NATIVE)
+    return fail(DKV_ERR_UNSUPPORTED, "the naive prefill baseline needs a one-layer 16-bit cache");
+  std::lock_guard<std::mutex> lk(c->mu);
+  if ((st = set_device(c)) != DKV_OK) return st;
+  return prefill_impl(c, 0, x, T, wq, wk, wv, hidden, n_q_heads, out, c->k_dev, c->v_dev,
+                      stream, true);
 }
 
 dkv_status dkv_prefill(dkv_cache* c, const void* x, int T, const void* wq, const void* wk,

@@ -261,6 +261,8 @@ struct PrefillParams {
   int nchunks;       // chunks per sequence (max over the batch)
   float scale_log2;
   CacheLayout lay;   // rows of k_read / v_read / k_host / v_host
+  int naive;         // baseline: every (Q tile, chunk) pair fetches the chunk again
+  int kv_fp8;        // caches hold 8-bit E4M3 (bf16 activations)
   int len[kMaxBatch];
 };
 

@@ -29,6 +29,10 @@
 // epilogue groups of four (one warp per TMEM lane quarter, one row per
 // thread): group 0 takes the even Q tiles, group 1 the odd ones.  Every wait
 // is bounded.
+#include <cuda_fp8.h>
+
+#include <type_traits>
+
 #include "tc_common.cuh"
 
 namespace dkv {
@@ -108,6 +112,10 @@ struct TcArgs {
   int* part_k;      // [nchunks, B*Hkv]
   DeviceStatus* status;
   int B, T, H, Hq, Hkv, nchunks;
+  // Q tiles per CTA.  The fused prefill gives each CTA every Q tile of its
+  // chunk (tile_groups = 1); the naive baseline gives each CTA one group of
+  // tiles_per_group tiles, so the chunk is fetched once per group.
+  int tile_groups, tiles_per_group;
   CacheLayout lay;  // rows of the caches (dense or paged)
   float scale_log2;
   int len[kMaxBatch];
@@ -151,7 +159,42 @@ __device__ __forceinline__ uint4 pack8(const uint32_t* r, float mul) {
   return o;
 }
 
-template <typename T, int D, int G>
+// Cache element C: the activation type T, or 8-bit E4M3 (bf16 activations).
+// E4M3 rows of the host cache land in a staging slot of the stationary tile
+// (the part of row r that the converted row r overwrites last) and are
+// converted in place: K to T for the Q.K^T MMA, V to fp16 for P.V.
+template <typename C>
+constexpr bool kE4M3 = sizeof(C) == 1;
+
+// Byte offset, inside one K or V tile, of the E4M3 staging slot of row r: the
+// last 128-byte region of the row for D = 128, the upper 64 bytes of its
+// single region for D = 64.  Converting row r reads the whole slot before it
+// writes row r, and no other row's output touches it.
+template <int D>
+__device__ __forceinline__ int e4m3_slot(int r) {
+  return (D / 64 - 1) * kRegKV + r * 128 + (D == 64 ? 64 : 0);
+}
+
+// Eight E4M3 values (the low 8 bytes of `w`, lower address first) as T or fp16 bits.
+template <typename T>
+__device__ __forceinline__ uint4 e4m3x8_to(uint2 w) {
+  const uint32_t in[2] = {w.x, w.y};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t two = (in[i / 2] >> (16 * (i % 2))) & 0xFFFFu;
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+    if constexpr (std::is_same<T, __half>::value) {
+      o[i] = (uint32_t)h.x | ((uint32_t)h.y << 16);
+    } else {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+      o[i] = tc::pack2<T>(f.x, f.y);   // exact: E4M3 values are bf16 values
+    }
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+template <typename T, typename C, int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_x,
@@ -182,8 +225,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(smem + Cfg::kOffBar);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // unit: (b, KV head, chunk) for the fused prefill; (b, KV head, Q tile
+  // group, chunk) with the chunks fastest for the naive baseline, the order in
+  // which a Q-stationary kernel would stream them
   const int c = blockIdx.x % a.nchunks;
-  const int bh = blockIdx.x / a.nchunks;
+  const int tg = (blockIdx.x / a.nchunks) % a.tile_groups;
+  const int bh = blockIdx.x / (a.nchunks * a.tile_groups);
   const int kvh = bh % a.Hkv, b = bh / a.Hkv;
   const int P = a.len[b];
   const int S = P + a.T;
@@ -194,8 +241,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool has_new = k0 + kC > P;            // rows [nhost, C) are projected here
   const int pass0 = nhost / 128;               // first 128-row projection pass with new rows
   const int npass = has_new ? 2 - pass0 : 0;
-  const int t_lo = max(0, k0 - P);             // first token that sees this chunk
-  const int ntiles = (a.T - t_lo + TQ - 1) / TQ;
+  const int t_vis = max(0, k0 - P);            // first token that sees this chunk
+  const int tile0 = tg * a.tiles_per_group;    // this CTA's first Q tile of the chunk
+  if (tile0 * TQ >= a.T - t_vis) return;       // uniform, before any barrier
+  const int t_lo = t_vis + tile0 * TQ;         // first token of this CTA's tiles
+  const int ntiles = min((a.T - t_lo + TQ - 1) / TQ, a.tiles_per_group);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -230,15 +280,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ loader
     // (a) cached rows of the chunk: host -> shared, 16-byte cp.async, swizzled.
     {
-      const T* kg = static_cast<const T*>(a.k_read);
-      const T* vg = static_cast<const T*>(a.v_read);
-      constexpr int CPR = D / 8;  // 16-byte chunks per row
+      const C* kg = static_cast<const C*>(a.k_read);
+      const C* vg = static_cast<const C*>(a.v_read);
+      constexpr int EPC = 16 / sizeof(C);  // elements per 16-byte chunk
+      constexpr int CPR = D / EPC;         // 16-byte chunks per row
       const int rows = has_new ? nhost : kC;  // zero-fill the tail when nothing is projected
       for (int i = lane; i < rows * CPR; i += 32) {
         const int r = i / CPR, cc = i % CPR;
-        const int off = swz(r, cc, kRegKV);
+        const int off = kE4M3<C> ? e4m3_slot<D>(r) + cc * 16 : swz(r, cc, kRegKV);
         const bool ok = r < nhost;
-        const size_t src = ok ? a.lay.row(b, kvh, k0 + r, D) + cc * 8 : 0;
+        const size_t src = ok ? a.lay.row(b, kvh, k0 + r, D) + cc * EPC : 0;
         cp_async16(ks + off, kg + src, ok ? 16 : 0);
         cp_async16(vs + off, vg + src, ok ? 16 : 0);
       }
@@ -403,21 +454,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = (pass0 + ps) * 128 + row;  // key row within the chunk
       const int key = k0 + r;
       const bool mine = r >= nhost;            // this row is a new key projected here
-      const bool append = mine && key < S;
+      const bool append = mine && key < S && tg == 0;  // appended once per chunk
       uint8_t* tile = hh ? vs : ks;
       // (the row is looked up only where it exists: key < S)
-      T* host = append ? static_cast<T*>(hh ? a.v_host : a.k_host) + a.lay.row(b, kvh, key, D)
+      C* host = append ? static_cast<C*>(hh ? a.v_host : a.k_host) + a.lay.row(b, kvh, key, D)
                        : nullptr;
 #pragma unroll 1
       for (int part = 0; part < D / 32; ++part) {
         uint32_t v[32];
         tc::tmem_ld32(tmem + lane_off + hh * D + part * 32, v);
         tc::tmem_wait_ld();
+        if constexpr (kE4M3<C>) {
+          // the fp32 sums rounded once to E4M3 (nearest, saturating) are the
+          // appended row; the tile holds those values (K as T, V as fp16)
+          uint32_t e[8];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 o = pack8<T>(v + q * 8, 1.f);
-          if (mine) *reinterpret_cast<uint4*>(tile + swz(r, part * 4 + q, kRegKV)) = o;
-          if (append) *reinterpret_cast<uint4*>(host + part * 32 + q * 8) = o;  // the append
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+                make_float2(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1])),
+                __NV_SATFINITE, __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+                make_float2(__uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])),
+                __NV_SATFINITE, __NV_E4M3);
+            e[q] = lo | (hi << 16);
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint2 w = make_uint2(e[2 * q], e[2 * q + 1]);
+            const uint4 o = hh ? e4m3x8_to<__half>(w) : e4m3x8_to<T>(w);
+            if (mine) *reinterpret_cast<uint4*>(tile + swz(r, part * 4 + q, kRegKV)) = o;
+          }
+          if (append) {  // the append: 32 bytes
+            reinterpret_cast<uint4*>(host + part * 32)[0] = make_uint4(e[0], e[1], e[2], e[3]);
+            reinterpret_cast<uint4*>(host + part * 32)[1] = make_uint4(e[4], e[5], e[6], e[7]);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 o = pack8<T>(v + q * 8, 1.f);
+            if (mine) *reinterpret_cast<uint4*>(tile + swz(r, part * 4 + q, kRegKV)) = o;
+            if (append) *reinterpret_cast<uint4*>(host + part * 32 + q * 8) = o;  // the append
+          }
         }
       }
       tc::fence_before_sync();
@@ -426,7 +503,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // the host rows have landed (loader's cp.async tracked by kv_host)
     wait_or_abort(&bars->kv_host, 0, bars, a.status, kSiteFull);
-    if (hh == 1) {
+    if constexpr (kE4M3<C>) {
+      // E4M3 host rows [0, nhost): group 0 converts K to T, group 1 V to
+      // fp16, one row per thread and pass, from the row's staging slot.  No
+      // chunk scale: E4M3 magnitudes stay below 448.
+      uint8_t* tile = hh ? vs : ks;
+#pragma unroll 1
+      for (int rr = 0; rr < 2; ++rr) {
+        const int r = rr * 128 + row;
+        if (r >= nhost) break;
+        uint4 in[D / 16];
+#pragma unroll
+        for (int cc = 0; cc < D / 16; ++cc)
+          in[cc] = *reinterpret_cast<const uint4*>(tile + e4m3_slot<D>(r) + cc * 16);
+#pragma unroll
+        for (int cc = 0; cc < D / 16; ++cc) {
+          const uint2 w0 = make_uint2(in[cc].x, in[cc].y), w1 = make_uint2(in[cc].z, in[cc].w);
+          *reinterpret_cast<uint4*>(tile + swz(r, 2 * cc, kRegKV)) =
+              hh ? e4m3x8_to<__half>(w0) : e4m3x8_to<T>(w0);
+          *reinterpret_cast<uint4*>(tile + swz(r, 2 * cc + 1, kRegKV)) =
+              hh ? e4m3x8_to<__half>(w1) : e4m3x8_to<T>(w1);
+        }
+      }
+      if (hh == 1 && warp == 6 && lane == 0 && tg == 0)
+        a.part_k[(size_t)c * a.B * a.Hkv + bh] = 0;
+    } else if (hh == 1) {
       // P.V runs in fp16 (P keeps 11 significant bits).  For bf16 inputs the
       // stationary V chunk is converted to fp16 in place, times 2^-k with k the
       // smallest power making max|V| < 2^15 (k = 0 unless V is huge); the
@@ -473,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (warp == 6 && lane == 0) a.part_k[(size_t)c * a.B * a.Hkv + bh] = k;
+      if (warp == 6 && lane == 0 && tg == 0) a.part_k[(size_t)c * a.B * a.Hkv + bh] = k;
     }
     tc::fence_proxy_async_smem();  // generic/cp.async smem writes -> tensor core reads
     tc::fence_before_sync();
@@ -669,12 +770,12 @@ __global__ void __launch_bounds__(128) prefill_combine_tc_kernel(
   const int last = (len.v[b] + t) / kC;
   if (*(const volatile int*)&status->code != 0) {
     if (active) {
-      uint32_t r[16];
+      uint32_t nan[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(NAN);
+      for (int e = 0; e < 16; ++e) nan[e] = __float_as_uint(NAN);
       uint4* dst = reinterpret_cast<uint4*>(out + row * D) + 2 * sub;
-      dst[0] = pack8<T>(r, 1.f);
-      dst[1] = pack8<T>(r + 8, 1.f);
+      dst[0] = pack8<T>(nan, 1.f);
+      dst[1] = pack8<T>(nan + 8, 1.f);
     }
     return;
   }
@@ -717,11 +818,11 @@ __global__ void __launch_bounds__(128) prefill_combine_tc_kernel(
   }
 }
 
-template <typename T, int D, int G>
+template <typename T, typename C, int D, int G>
 cudaError_t launch_t(const TcArgs& args, const CUtensorMap& mq, const CUtensorMap& mx,
                      const CUtensorMap& mk, const CUtensorMap& mv, void* out, cudaStream_t s,
                      const KernelTimer& timer) {
-  auto k = prefill_tc_kernel<T, D, G>;
+  auto k = prefill_tc_kernel<T, C, D, G>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        smem_request<D>());
   if (e != cudaSuccess) return e;
@@ -729,7 +830,7 @@ cudaError_t launch_t(const TcArgs& args, const CUtensorMap& mq, const CUtensorMa
   if (!make_tmap_partial(&mpo, args.part_o, D, (uint64_t)args.T * G,
                          (uint64_t)args.nchunks * args.B * args.Hkv))
     return cudaErrorInvalidValue;
-  const int units = args.B * args.Hkv * args.nchunks;
+  const int units = args.B * args.Hkv * args.nchunks * args.tile_groups;
   timer.before(s);
   k<<<units, kThreads, smem_request<D>(), s>>>(mq, mx, mk, mv, mpo, args);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -774,10 +875,20 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, const void* wq,
   a.part_o = p.part_o; a.part_lse = p.part_lse; a.part_k = p.part_k; a.status = p.status;
   a.B = p.B; a.T = p.T; a.H = p.H; a.Hq = p.Hq; a.Hkv = p.Hkv; a.lay = p.lay;
   a.nchunks = p.nchunks; a.scale_log2 = p.scale_log2;
+  const int tiles = (p.T + kBQ / G - 1) / (kBQ / G);  // Q tiles of the longest chunk
+  a.tiles_per_group = p.naive ? 1 : tiles;
+  a.tile_groups = p.naive ? tiles : 1;
   for (int i = 0; i < kMaxBatch; ++i) a.len[i] = p.len[i];
 #define DKV_TC(TT, DD, GG) \
-  if (D == DD && G == GG) e = launch_t<TT, DD, GG>(a, mq, mx, mk, mv, p.out, s, timer); else
-  if (dtype == DKV_BF16) {
+  if (D == DD && G == GG) e = launch_t<TT, TT, DD, GG>(a, mq, mx, mk, mv, p.out, s, timer); else
+#define DKV_TC8(DD, GG) \
+  if (D == DD && G == GG) \
+    e = launch_t<__nv_bfloat16, __nv_fp8_e4m3, DD, GG>(a, mq, mx, mk, mv, p.out, s, timer); else
+  if (p.kv_fp8) {
+    if (dtype != DKV_BF16) return cudaErrorInvalidValue;
+    DKV_TC8(64, 1) DKV_TC8(64, 2) DKV_TC8(64, 4) DKV_TC8(64, 8)
+    DKV_TC8(128, 1) DKV_TC8(128, 2) DKV_TC8(128, 4) DKV_TC8(128, 8) e = cudaErrorInvalidValue;
+  } else if (dtype == DKV_BF16) {
     DKV_TC(__nv_bfloat16, 64, 1) DKV_TC(__nv_bfloat16, 64, 2) DKV_TC(__nv_bfloat16, 64, 4)
     DKV_TC(__nv_bfloat16, 64, 8) DKV_TC(__nv_bfloat16, 128, 1) DKV_TC(__nv_bfloat16, 128, 2)
     DKV_TC(__nv_bfloat16, 128, 4) DKV_TC(__nv_bfloat16, 128, 8) e = cudaErrorInvalidValue;
@@ -787,6 +898,7 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, const void* wq,
     e = cudaErrorInvalidValue;
   }
 #undef DKV_TC
+#undef DKV_TC8
   if (e == cudaSuccess && launches) *launches += 3;
   return e;
 }
