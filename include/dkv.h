@@ -100,6 +100,8 @@ typedef struct {
     int max_pages_per_seq;  /* paged caches: page-table entries per sequence */
     int layers;             /* layered caches: layers held (1 otherwise) */
     int kv_format;          /* dkv_kv_format of the K/V elements */
+    int numa_node_wanted;   /* host NUMA node attached to the cache's GPU (-1: unknown) */
+    int numa_node;          /* node holding the cache's first page (-1: unknown) */
 } dkv_cache_info_t;
 
 /* Allocate a K cache and a V cache of [batch][n_kv_heads][max_tokens][head_dim]
@@ -165,6 +167,22 @@ dkv_status dkv_cache_set_page_table(dkv_cache* cache, const int32_t* table);
  * sure no enqueued work still uses the cache.  A handle already freed (or
  * never returned by dkv_cache_alloc) gives INVALID_ARG. */
 dkv_status dkv_free(dkv_cache* cache);
+
+/* The host NUMA node sysfs reports for a PCI device, given its bus id as
+ * cudaDeviceGetPCIBusId prints it ("0000:1B:00.0"), read from
+ * <sysfs_root>/bus/pci/devices/<id>/numa_node (sysfs_root null or "": /sys);
+ * -1 when unknown, absent or malformed.  Every cache allocation pins its pages
+ * with the calling thread's memory policy preferring the node of the current
+ * GPU (so each replica's cache sits next to its own host link; "Paper Notes:
+ * DirectKV", System Architecture, KV Cache Manager), then restores the policy;
+ * DKV_NUMA=0 in the environment turns that off.  dkv_cache_info reports the
+ * node wanted and the node the first page landed on. */
+int dkv_pci_numa_node(const char* pci_bus_id, const char* sysfs_root);
+
+/* Allocates and touches one page of ordinary host memory with the calling
+ * thread's policy preferring `node`, as the cache allocation does, and
+ * returns the node it landed on (-1 if unknown).  Needs no GPU. */
+int dkv_numa_probe(int node);
 
 /* Host addresses of the two caches ([B][Hkv][max_tokens][D] each), for
  * filling prefixes and reading back appended rows.  The host must not touch

@@ -52,3 +52,17 @@ def test_prefill_hbm_minimum():
 def test_decode_attention_flops():
     # 4 x B x Hq x (P + 1) x D: the new token attends to itself
     assert W["llama8b_decode"].attn_flops() == 4 * 8 * 32 * 32769 * 128
+
+
+def test_prefill_partial_rows_hand_worked():
+    """Partial rows of the KV-stationary prefill (256-key chunks): the 112
+    wholly cached chunks are seen by all 4096 tokens, new-token chunk i by
+    4096 - 256 i of them; 32 query heads; 260 bytes per row (fp16 o + lse)."""
+    import bench
+    w = W["llama8b_prefill"]
+    rows = (112 * 4096 + sum(4096 - 256 * i for i in range(16))) * 32
+    assert rows == 15_794_176
+    assert bench.prefill_partial_rows(w) == rows
+    assert rows * 260 == 4_106_485_760   # the combine's reads (ncu: 4,106,566,144 B)
+    q = W["llama8b_prefill_quarter"]
+    assert bench.prefill_partial_rows(q) == (28 * 1024 + 1024 + 768 + 512 + 256) * 32

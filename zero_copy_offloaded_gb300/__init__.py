@@ -27,7 +27,7 @@ __all__ = [
     "PagedKVCache", "LayeredKVCache", "dkv_cache_alloc_layered", "dkv_decode_layer",
     "dkv_prefill_layer", "dkv_step_graph_capture", "dkv_step_graph_launch",
     "dkv_cache_alloc_ex", "KV_FORMATS", "dkv_decode_noalloc", "dkv_decode_noalloc_status",
-    "dkv_decode_noalloc_debug_withhold",
+    "dkv_decode_noalloc_debug_withhold", "dkv_pci_numa_node", "dkv_numa_probe",
 ]
 
 BF16 = 0
@@ -59,7 +59,8 @@ class _CacheInfo(ctypes.Structure):
                 ("head_dim", ctypes.c_int), ("max_tokens", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("page_tokens", ctypes.c_int),
                 ("num_pages", ctypes.c_int), ("max_pages_per_seq", ctypes.c_int),
-                ("layers", ctypes.c_int), ("kv_format", ctypes.c_int)]
+                ("layers", ctypes.c_int), ("kv_format", ctypes.c_int),
+                ("numa_node_wanted", ctypes.c_int), ("numa_node", ctypes.c_int)]
 
 
 class _CacheDesc(ctypes.Structure):
@@ -136,6 +137,10 @@ def lib(build_if_missing: bool = False):
     L.dkv_last_error.restype = ctypes.c_char_p
     L.dkv_last_launch_count.argtypes = []
     L.dkv_last_launch_count.restype = ctypes.c_int
+    L.dkv_pci_numa_node.argtypes = [ctypes.c_char_p, ctypes.c_char_p]
+    L.dkv_pci_numa_node.restype = ctypes.c_int
+    L.dkv_numa_probe.argtypes = [ctypes.c_int]
+    L.dkv_numa_probe.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -275,6 +280,16 @@ def dkv_cache_info(h) -> dict:
     i = _CacheInfo()
     _check(lib().dkv_cache_info(h, ctypes.byref(i)), "dkv_cache_info")
     return {f: getattr(i, f) for f, _ in _CacheInfo._fields_}
+
+
+def dkv_pci_numa_node(pci_bus_id: str, sysfs_root: str | None = None) -> int:
+    """Host NUMA node of a PCI device (-1 if unknown); see include/dkv.h."""
+    return lib().dkv_pci_numa_node(pci_bus_id.encode(),
+                                   sysfs_root.encode() if sysfs_root else None)
+
+
+def dkv_numa_probe(node: int) -> int:
+    return lib().dkv_numa_probe(int(node))
 
 
 def dkv_cache_reserve(h, n_q_heads, max_new_tokens):

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libdkv.so")
 SOURCES = ["dkv_api.cu", "decode.cu", "probes.cu", "decode_noalloc.cu", "gemm_tc.cu",
-           "prefill_tc.cu"]
+           "prefill_tc.cu", "numa_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

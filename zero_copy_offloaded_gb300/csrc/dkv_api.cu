@@ -24,6 +24,7 @@
 #include <vector>
 
 #include "dkv_internal.cuh"
+#include "numa_host.h"
 
 using namespace dkv;
 
@@ -86,6 +87,7 @@ struct dkv_cache {
   int* pages_dev;              // device copy read by the kernels
   // cache element format: DKV_KV_NATIVE (the dtype, 2 bytes) or DKV_KV_E4M3
   int kv_format, kv_eb;
+  int numa_node_wanted, numa_node;  // host node of the GPU; node of the first cache page
   // layered caches: `layers` caches of layer_elems elements each for K and V
   int layers;
   size_t layer_elems;
@@ -365,19 +367,24 @@ static dkv_status alloc_common(dkv_cache** out, int batch, int n_kv_heads, int h
   const size_t bytes = rows * head_dim * kv_eb * layers;
   void* kh = nullptr;
   void* vh = nullptr;
-  e = cudaHostAlloc(&kh, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return fail(DKV_ERR_ALLOC, "cudaHostAlloc(%zu) for K: %s", bytes, cudaGetErrorString(e));
+  // pinned on the host NUMA node attached to this GPU, where known
+  const int node = device_numa_node(dev);
+  {
+    NumaScope scope(node);
+    e = cudaHostAlloc(&kh, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(DKV_ERR_ALLOC, "cudaHostAlloc(%zu) for K: %s", bytes, cudaGetErrorString(e));
+    }
+    e = cudaHostAlloc(&vh, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      cudaFreeHost(kh);
+      return fail(DKV_ERR_ALLOC, "cudaHostAlloc(%zu) for V: %s", bytes, cudaGetErrorString(e));
+    }
+    memset(kh, 0, bytes);
+    memset(vh, 0, bytes);
   }
-  e = cudaHostAlloc(&vh, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    cudaFreeHost(kh);
-    return fail(DKV_ERR_ALLOC, "cudaHostAlloc(%zu) for V: %s", bytes, cudaGetErrorString(e));
-  }
-  memset(kh, 0, bytes);
-  memset(vh, 0, bytes);
   void* kd = nullptr;
   void* vd = nullptr;
   if ((e = cudaHostGetDevicePointer(&kd, kh, 0)) != cudaSuccess ||
@@ -442,6 +449,8 @@ static dkv_status alloc_common(dkv_cache** out, int batch, int n_kv_heads, int h
   c->layer_elems = rows * head_dim;
   c->kv_format = kv_format;
   c->kv_eb = kv_eb;
+  c->numa_node_wanted = node;
+  c->numa_node = page_numa_node(kh);
   c->len_dev = len_dev;
   c->len_dev_stale = false;
   c->step_exec = nullptr;
@@ -622,6 +631,8 @@ dkv_status dkv_cache_info(const dkv_cache* c, dkv_cache_info_t* info) {
   info->max_pages_per_seq = c->max_pages;
   info->layers = c->layers;
   info->kv_format = c->kv_format;
+  info->numa_node_wanted = c->numa_node_wanted;
+  info->numa_node = c->numa_node;
   return DKV_OK;
 }
 
