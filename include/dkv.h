@@ -235,7 +235,10 @@ dkv_status dkv_decode_layer(dkv_cache* cache, int layer, const void* x, const vo
  * the graph keeps those pointers and the kernel configuration chosen now, and
  * reads the sequence lengths from device memory at run time, so every launch
  * appends at the lengths of its own step.  Captures on a stream of the
- * library's own; replaces an earlier capture.  Errors: as dkv_decode, CUDA
+ * library's own; replaces an earlier capture.  A later call that needs a
+ * larger workspace (a longer prefill, say) discards the capture, since the
+ * graph holds workspace addresses; dkv_step_graph_launch then returns
+ * INVALID_ARG until the step is captured again.  Errors: as dkv_decode, CUDA
  * (the capture or instantiation failed). */
 dkv_status dkv_step_graph_capture(dkv_cache* cache, int hidden, int n_q_heads,
                                   const void* const* x, const void* const* wq,

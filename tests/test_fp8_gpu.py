@@ -114,7 +114,7 @@ def e4m3_ulp_distance(a, b):
     return np.abs(ordered(a) - ordered(b))
 
 
-def check_prefill_e4m3(case, out, ref, label):
+def check_prefill_e4m3(case, out, ref, label, rows=None):
     """The fused prefill's projection sums on the tensor cores in another
     order than the oracle's fp32 chain and then rounds once to E4M3.  So each
     appended code is the oracle's, or one step away where the exact sum lies
@@ -154,19 +154,30 @@ def check_prefill_e4m3(case, out, ref, label):
         assert np.array_equal(kh[b, :, :p], case.k0[b, :, :p])
         assert np.array_equal(vh[b, :, :p], case.v0[b, :, :p])
         assert np.all(kh[b, :, p + T:] == case.canary) and np.all(vh[b, :, p + T:] == case.canary)
-    # the oracle's attention over the cache as written
-    att = np.zeros((w.B, T, w.Hq, w.D))
-    for b in range(w.B):
+    # the oracle's attention over the cache as written (all rows, or the
+    # sampled (b, t) rows)
+    want = [(b, t) for b in range(w.B) for t in range(T)] if rows is None else list(rows)
+    by_b = {}
+    for b, t in want:
+        by_b.setdefault(b, []).append(t)
+    got_all = out_f64(out, w.dtype).reshape(w.B, T, w.Hq, w.D)
+    att, got = [], []
+    for b, ts in by_b.items():
         p = int(case.lens[b])
+        ts = np.asarray(ts)
+        a = np.zeros((len(ts), w.Hq, w.D))
         for kvh in range(w.Hkv):
             kf = oracle.decode_e4m3(kh[b, kvh, :p + T])
             vf = oracle.decode_e4m3(vh[b, kvh, :p + T])
-            q = oracle.decode_bits(ref["q"][b, :, kvh * G:(kvh + 1) * G], w.dtype)
-            pos = np.repeat(p + np.arange(T), G)
-            att[b, :, kvh * G:(kvh + 1) * G] = oracle.attend(
-                kf, vf, q.reshape(-1, w.D), pos).reshape(T, G, w.D)
-    got = out_f64(out, w.dtype).reshape(w.B, T, w.Hq, w.D)
-    mx, mr = assert_close_beyond_rounding(got, att, w.dtype, label)
+            q = oracle.decode_bits(ref["q"][b][np.ix_(ts, range(kvh * G, (kvh + 1) * G))],
+                                   w.dtype)
+            pos = np.repeat(p + ts, G)
+            a[:, kvh * G:(kvh + 1) * G] = oracle.attend(
+                kf, vf, q.reshape(-1, w.D), pos).reshape(len(ts), G, w.D)
+        att.append(a)
+        got.append(got_all[b, ts])
+    mx, mr = assert_close_beyond_rounding(np.concatenate(got), np.concatenate(att), w.dtype,
+                                          label)
     return mx, mr, exact_n / tot
 
 
@@ -206,5 +217,24 @@ def test_fp8_prefill_paged_spiky_then_decode():
         assert_close_beyond_rounding(out_f64(out2, w.dtype).reshape(w.B, w.Hq, w.D),
                                      ref2["out"].reshape(w.B, w.Hq, w.D), w.dtype,
                                      "decode after e4m3 prefill")
+    finally:
+        case.free()
+
+
+@pytest.mark.slow
+def test_fp8_prefill_llama8b_full_size_sampled_rows():
+    """The Llama-3-8B-shaped chunked prefill (T=4096 over P=28672) on an E4M3
+    cache, as the benchmark runs it: every appended code checked, attention
+    on 512 seeded query rows including the first and last token of every
+    chunk that holds new tokens."""
+    from .test_prefill_gpu import _edge_and_random_rows
+    w = wl.WORKLOADS["llama8b_prefill"]
+    case = Case(w, kv_format="e4m3")
+    try:
+        out = case.run_prefill()
+        rows = _edge_and_random_rows(w, 512, seed=1)
+        ref = case.oracle(rows=rows[:1])  # q, k_new and v_new of every token
+        _, _, exact = check_prefill_e4m3(case, out, ref, "e4m3 llama8b_prefill", rows=rows)
+        assert exact > 0.99
     finally:
         case.free()

@@ -200,3 +200,26 @@ def test_layered_errors():
         assert ei.value.name == "DKV_ERR_CAPACITY"
     finally:
         c.free()
+
+
+def test_captured_step_discarded_when_the_workspace_grows():
+    """A prefill that needs a larger workspace discards the captured step
+    (its addresses would be stale): the launch asks for a new capture."""
+    import torch
+    w = wl.Workload("t", "decode", B=1, H=128, Hq=8, Hkv=2, D=64, P=100, seed=3)
+    lay = Layers(2, w, [100], 1200)
+    try:
+        outs = [_decode_out(w) for _ in range(2)]
+        xs = [d["x"].reshape(w.B, 1, w.H) for d in lay.dev]
+        lay.cache.capture_step(xs, [d["wq"] for d in lay.dev], [d["wk"] for d in lay.dev],
+                               [d["wv"] for d in lay.dev], w.Hq, outs)
+        d = lay.dev[0]
+        xp = torch.zeros((1, 1000, w.H), dtype=torch_dtype(w.dtype), device="cuda")
+        op = torch.empty((1, 1000, w.Hq, w.D), dtype=torch_dtype(w.dtype), device="cuda")
+        lay.cache.prefill_layer(0, xp, d["wq"], d["wk"], d["wv"], w.Hq, op)
+        lay.cache.sync()
+        with pytest.raises(dkv.DkvError) as ei:
+            lay.cache.launch_step()
+        assert ei.value.name == "DKV_ERR_INVALID_ARG"
+    finally:
+        lay.free()

@@ -113,6 +113,12 @@ dkv_status ensure_ws(dkv_cache* c, size_t need) {
   if (c->ws.bytes >= need) return DKV_OK;
   cudaError_t e = cudaStreamSynchronize(c->last_stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  // a captured step holds addresses in the old block: it is discarded (the
+  // next dkv_step_graph_launch asks for a new capture)
+  if (c->step_exec) {
+    cudaGraphExecDestroy(c->step_exec);
+    c->step_exec = nullptr;
+  }
   if (c->ws.base) cudaFree(c->ws.base);
   c->ws.base = nullptr;
   c->ws.bytes = 0;
