@@ -284,11 +284,12 @@ dkv_status dkv_sync_status(dkv_cache* cache, void* stream);
 dkv_status dkv_cache_set_tuning(dkv_cache* cache, int splits, int tile_n, int stages);
 
 /* Test hook for the failure-detection path: while enabled, the producer
- * warps of every dkv_decode on this cache never signal their first host tile,
- * so the consumers' bounded wait expires after about one second; the kernel
- * drains its own copies and returns, and dkv_sync_status reports
- * DKV_ERR_TIMEOUT.  The output of such a call is NaN; the cache rows before
- * the append are untouched and the context stays usable. */
+ * warps of every dkv_decode on this cache never signal their first host tile
+ * (and the loader of every dkv_prefill never signals its chunk's host rows),
+ * so a bounded wait expires after about one second; the kernel drains its own
+ * copies and returns, and dkv_sync_status reports DKV_ERR_TIMEOUT.  The output
+ * of such a call is NaN; the cache rows before the append are untouched and
+ * the context stays usable. */
 dkv_status dkv_cache_debug_withhold(dkv_cache* cache, int enable);
 
 const char* dkv_status_str(dkv_status s);

@@ -37,3 +37,33 @@ def test_withheld_tile_times_out_then_recovers():
         case.cache.sync()  # no stale timeout left behind
     finally:
         case.free()
+
+
+def test_withheld_prefill_rows_time_out_then_recover():
+    """The prefill's loader withholds the arrival of its chunk's host rows:
+    the bounded waits give up, DKV_ERR_TIMEOUT is reported, the outputs are
+    NaN (the combine sees the status), the prefix is intact, and the next
+    prefill on the same context is correct."""
+    import torch
+    import zero_copy_offloaded_gb300 as dkv
+    from .test_prefill_gpu import check_prefill
+    w = wl.Workload("t", "prefill", B=2, H=128, Hq=8, Hkv=2, D=128, P=600, T=70, seed=37)
+    case = Case(w, s_max=w.P + w.T + 3)
+    try:
+        dkv.dkv_cache_debug_withhold(case.cache.h, True)
+        out = case.out_tensor(w.T)
+        out.zero_()
+        case.cache.prefill(case.x, case.wq, case.wk, case.wv, w.Hq, out)
+        with pytest.raises(dkv.DkvError) as ei:
+            case.cache.sync()
+        assert ei.value.name == "DKV_ERR_TIMEOUT"
+        assert torch.isnan(out.float()).all()
+        assert np.array_equal(case.cache.k_host[:, :, : w.P], case.k0[:, :, : w.P])
+        dkv.dkv_cache_debug_withhold(case.cache.h, False)
+        case.cache.k_host[...] = case.k0
+        case.cache.v_host[...] = case.v0
+        case.cache.set_lengths(case.lens.astype(np.int32))
+        out = case.run_prefill()
+        check_prefill(case, out, case.oracle(), "prefill after recovery")
+    finally:
+        case.free()

@@ -867,6 +867,7 @@ dkv_status prefill_impl(dkv_cache* c, int layer, const void* x, int T, const voi
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   p.lay = layout_of(c);
   p.naive = naive ? 1 : 0;
+  p.debug_withhold = c->debug_withhold;
   p.kv_fp8 = c->kv_format == DKV_KV_E4M3;
   fill_lens(p.len, c->len);
   cudaStream_t s = static_cast<cudaStream_t>(stream);

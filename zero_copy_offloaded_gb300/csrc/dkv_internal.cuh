@@ -263,6 +263,7 @@ struct PrefillParams {
   CacheLayout lay;   // rows of k_read / v_read / k_host / v_host
   int naive;         // baseline: every (Q tile, chunk) pair fetches the chunk again
   int kv_fp8;        // caches hold 8-bit E4M3 (bf16 activations)
+  int debug_withhold;  // test hook for the bounded-wait path
   int len[kMaxBatch];
 };
 

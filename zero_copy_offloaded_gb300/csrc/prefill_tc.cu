@@ -90,6 +90,11 @@ constexpr int smem_request() {
 
 struct Bars {
   uint64_t q_full[2], q_empty[2], kv_host, kv_ready, pr_full[2], pr_empty[2], pr_done, pr_drain;
+  // one phase: every projection pass's MMAs have completed (the loader's
+  // signal that the staging it aliases with the Q buffers is free; pr_done
+  // has a phase per pass, and a thread outside the pass hand-offs could see
+  // both complete before its first test and then wait on the wrong phase)
+  uint64_t pr_all;
   // per TMEM region: S computed, P written (4 warps), O computed, O read out
   // (4 warps: the region may take the next tile's S)
   uint64_t s_full[2], p_full[2], o_full[2], r_free[2];
@@ -97,6 +102,7 @@ struct Bars {
   // the previous tile (the other group's), one arrival per tile
   uint64_t st_free[4];
   uint64_t vsync;     // rendezvous of the four warps converting V
+  uint64_t mma_drain; // after a give-up: every MMA the issuing thread started has completed
   uint32_t tmem_base;
   volatile int abort;
   float vmax[4];
@@ -116,6 +122,7 @@ struct TcArgs {
   // chunk (tile_groups = 1); the naive baseline gives each CTA one group of
   // tiles_per_group tiles, so the chunk is fetched once per group.
   int tile_groups, tiles_per_group;
+  int debug_withhold;  // test hook: the loader never signals the chunk's host rows
   CacheLayout lay;  // rows of the caches (dense or paged)
   float scale_log2;
   int len[kMaxBatch];
@@ -127,6 +134,14 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
   if (!bars->abort) record_timeout(st, site);
   bars->abort = 1;
   return false;
+}
+
+// Waits, for at most the wait budget and whatever the abort flag says, for
+// the phase with the given parity of a barrier that a TMA load completes.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t deadline = global_timer_ns() + kWaitBudgetNs;
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() > deadline) return;
 }
 
 // Warp-uniform bounded wait (tcgen05.ld / st after it need the whole warp).
@@ -264,8 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->kv_host, 32);
     mbar_init(&bars->kv_ready, 8);
     mbar_init(&bars->pr_done, 1);
+    mbar_init(&bars->pr_all, 1);
     mbar_init(&bars->pr_drain, 8);
     mbar_init(&bars->vsync, 4);
+    mbar_init(&bars->mma_drain, 1);
     bars->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -293,9 +310,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         cp_async16(ks + off, kg + src, ok ? 16 : 0);
         cp_async16(vs + off, vg + src, ok ? 16 : 0);
       }
-      cp_async_arrive_noinc(&bars->kv_host);
+      // (the test hook withholds this arrival: every role's bounded wait then
+      // gives up, a timeout is recorded and the combine writes NaN)
+      if (!a.debug_withhold) cp_async_arrive_noinc(&bars->kv_host);
     }
     if (lane == 0) {
+      // last load issued into each projection stage / Q buffer (-1: none)
+      int last_g[2] = {-1, -1}, last_q[2] = {-1, -1};
       tc::prefetch_tmap(&map_q);
       // (b) projection operands, one 128-row pass at a time: x rows, [Wk | Wv]
       if (has_new) {
@@ -312,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* pa = qs + s * Cfg::kProjStage;
             uint8_t* pb = pa + Cfg::kProjA;
             tc::mbar_expect_tx(&bars->pr_full[s], Cfg::kProjStage);
+            last_g[s] = g;
             tc::tma_load_2d(pa, &map_x, kb * 64, xrow, &bars->pr_full[s]);
 #pragma unroll
             for (int r = 0; r < DR; ++r) {
@@ -323,10 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // the Q buffers alias the projection staging: wait until every pass
-        // has consumed it (phases in order: a parity wait on a phase that has
-        // not started yet would return at once)
-        for (int ps = 0; ps < npass; ++ps)
-          if (!wait_or_abort(&bars->pr_done, ps & 1, bars, a.status, kSiteFull)) break;
+        // has consumed it
+        wait_or_abort(&bars->pr_all, 0, bars, a.status, kSiteFull);
       }
       // (c) Q tiles, double-buffered
       for (int i = 0; i < ntiles && !bars->abort; ++i) {
@@ -335,10 +355,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         const int tok = b * a.T + t_lo + i * TQ;
         tc::mbar_expect_tx(&bars->q_full[s], Cfg::kQ);
+        last_q[s] = i;
 #pragma unroll
         for (int r = 0; r < DR; ++r)
           tc::tma_load_3d(qs + s * Cfg::kQ + r * kRegQ, &map_q, r * 64, kvh * G, tok,
                           &bars->q_full[s]);
+      }
+      if (bars->abort) {
+        // after a give-up nobody consumes the loads still in flight: let the
+        // last one into each buffer land before the CTA leaves (bounded)
+        for (int s = 0; s < 2; ++s) {
+          if (last_g[s] >= 0) drain_wait(&bars->pr_full[s], (last_g[s] >> 1) & 1);
+          if (last_q[s] >= 0) drain_wait(&bars->q_full[s], (last_q[s] >> 1) & 1);
+        }
       }
     }
     cp_async_wait_all();
@@ -369,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::mma_commit(&bars->pr_done);
         }
+        tc::mma_commit(&bars->pr_all);  // arrives once every MMA above has completed
       }
       // the stationary K/V tile is complete (host rows landed, new rows written)
       wait_or_abort(&bars->kv_ready, 0, bars, a.status, kSiteFull);
@@ -435,6 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           bars->abort = 1;
           break;
         }
+      }
+      if (bars->abort) {
+        // after a give-up, the MMAs already issued finish before TMEM is freed
+        tc::mma_commit(&bars->mma_drain);
+        drain_wait(&bars->mma_drain, 0);
       }
     }
     __syncwarp();
@@ -877,6 +912,7 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, const void* wq,
   a.nchunks = p.nchunks; a.scale_log2 = p.scale_log2;
   const int tiles = (p.T + kBQ / G - 1) / (kBQ / G);  // Q tiles of the longest chunk
   a.tiles_per_group = p.naive ? 1 : tiles;
+  a.debug_withhold = p.debug_withhold;
   a.tile_groups = p.naive ? tiles : 1;
   for (int i = 0; i < kMaxBatch; ++i) a.len[i] = p.len[i];
 #define DKV_TC(TT, DD, GG) \
