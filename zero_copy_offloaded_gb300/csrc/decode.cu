@@ -89,16 +89,23 @@ constexpr int kProducers = kProducerWarps * 32;
 constexpr int kThreads = kConsumers + kProducers;
 constexpr int kBarConsumers = 1;  // named barrier id for the consumer warps
 constexpr int kProjRows = 128;    // H rows per projection chunk
-constexpr int kProjCols = 64;     // columns per projection pass (multiple of 8)
+constexpr int kProjBlk = 32;      // weight columns per TMA block (64-byte rows)
+
+// Weight blocks a projection pass takes together: one thread per column and
+// the batch rows split over the threads that remain, at most 8 chains a
+// thread (kConsumers / 64 = 4 thread rows for two blocks, 8 for one).
+__host__ __device__ inline int proj_group_max(int B) { return B <= 32 ? 2 : 1; }
 
 constexpr int kSmemCap = 232448 - 1024;  // dynamic shared memory per CTA, with margin
 
 // Shared-memory layout (byte offsets), all derived from the launch shape.
-// The projection's weight / x staging gets as many chunk stages (4 down to
-// 2) as fit beside the tile ring: the in-order FMA chains wait on one chunk
-// at a time, so deeper staging keeps more HBM loads in flight.
+// The projection's staging gets as many chunk stages (4 down to 2) as fit
+// beside the tile ring; a stage holds the weight blocks of one 128-row chunk
+// ([block][128][32]) followed by x's matching columns for every sequence
+// ([B][128]), both written by TMA.  Deeper staging keeps more HBM loads in
+// flight under the in-order FMA chains.
 struct DecodeSmem {
-  int ring, bars, q, s, alpha, ml, red, wproj, xproj, flag, total, proj_stages, pbar;
+  int ring, bars, q, s, alpha, ml, red, proj, pstage, flag, total, proj_stages, pbar;
   int eb;  // bytes per cache element
   __host__ __device__ DecodeSmem(int D, int G, int N, int stages, int B, int eb_ = 2) : eb(eb_) {
     for (proj_stages = 4; proj_stages > 2; --proj_stages)
@@ -117,22 +124,14 @@ struct DecodeSmem {
     red = off; off += kConsumers * 2 * 4;
     off = (off + 15) & ~15;
     off = (off + 127) & ~127;
-    wproj = off; off += proj_stages * kProjRows * kProjCols * 2;
-    pbar = off; off += 8 * 8;
-    xproj = off; off += proj_stages * B * kProjRows * 2;
+    pstage = proj_group_max(B) * kProjRows * kProjBlk * 2 + B * kProjRows * 2;
+    proj = off; off += proj_stages * pstage;
+    pbar = off; off += 2 * 4 * 8;  // full[4], empty[4]
     flag = off; off += 16;
     total = off;
     return total;
   }
 };
-
-// cp.async.wait_group with the count known only at run time (2..4 stages).
-__device__ __forceinline__ void cp_async_wait_stages(int pending) {
-  if (pending >= 3) cp_async_wait_group<3>();
-  else if (pending == 2) cp_async_wait_group<2>();
-  else if (pending == 1) cp_async_wait_group<1>();
-  else cp_async_wait_group<0>();
-}
 
 template <typename T, int D>
 __device__ __forceinline__ const T* col_source(const DecodeParams& p, int col, int& which,
@@ -143,148 +142,167 @@ __device__ __forceinline__ const T* col_source(const DecodeParams& p, int col, i
   which = 2; local = col - nq - nk; return static_cast<const T*>(p.wv);
 }
 
-// Phase A: columns [c_begin, c_end) of [Wq | Wk | Wv] for all B sequences.
-// Each output is one fp32 FMA chain over j = 0..H-1 in order (each product of
-// two 16-bit floats is exact in fp32, so the chain equals summing the exact
-// products with one fp32 rounding per step), rounded once to T.
-template <typename T, typename C, int D>
-__device__ void project_columns(const DecodeParams& p, int c_begin, int c_end, uint8_t* smem,
-                                const DecodeSmem& L, int ctid, const CUtensorMap* mq,
-                                const CUtensorMap* mk, const CUtensorMap* mv, uint32_t& gdone,
-                                volatile int* abort_flag) {
-  uint64_t* pbar = reinterpret_cast<uint64_t*>(smem + L.pbar);
-  T* wbuf = reinterpret_cast<T*>(smem + L.wproj);   // [S][kProjRows][kProjCols]
-  T* xbuf = reinterpret_cast<T*>(smem + L.xproj);   // [S][B][kProjRows]
-  const int S = L.proj_stages;
-  const T* x = static_cast<const T*>(p.x);
-  const int B = p.B, H = p.H;
-  const int nchunks = (H + kProjRows - 1) / kProjRows;
-  for (int cb = c_begin; cb < c_end; cb += kProjCols) {
-    const int ncols = min(kProjCols, c_end - cb);  // multiple of 8
-    const int npairs = ncols / 2;
-    const int nbp = (B + 1) / 2;
-    const int ngroups = npairs * nbp;
-    for (int gbase = 0; gbase < ngroups; gbase += kConsumers) {
-      const int gi = gbase + ctid;
-      const bool active = gi < ngroups;
-      const int pair = active ? gi % npairs : 0;
-      const int b0 = active ? (gi / npairs) * 2 : 0;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+// One fp32 sum rounded once to a cache element.
+template <typename T, typename C>
+__device__ __forceinline__ void store_one(C* dst, float a) {
+  if constexpr (KVE<T, C>::EB == 1)
+    *reinterpret_cast<__nv_fp8_storage_t*>(dst) = __nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3);
+  else
+    *dst = DT<T>::from_f(a);
+}
 
-      // A pass over one whole 64-column block of one weight matrix takes its
-      // weight chunks by TMA (one 128 x 64 box each, off the load/store path
-      // the producers' host requests use); narrower passes use cp.async.
-      // TMA passes number their chunks with a running count g0 + c, which
-      // picks the stage and its barrier's phase.
-      int tw_which = 0, tw_local = 0;
-      (void)col_source<T, D>(p, cb, tw_which, tw_local);
-      const bool tma = p.proj_tma && ncols == kProjCols && (tw_local % kProjCols) == 0;
-      const CUtensorMap* tmap = tw_which == 0 ? mq : (tw_which == 1 ? mk : mv);
-      const uint32_t g0 = tma ? gdone : 0u;
-      auto issue = [&](int chunk, int buf) {
-        if (chunk >= nchunks) {  // keep one (empty) group per chunk slot
-          cp_async_commit();
-          return;
-        }
-        const int j0 = chunk * kProjRows;
-        const int rows = min(kProjRows, H - j0);
-        const int pieces_per_row = ncols / 8;
-        T* wdst = wbuf + buf * kProjRows * kProjCols;
-        if (tma) {
-          if (ctid == 0) {
-            tc::fence_proxy_async_smem();
-            tc::mbar_expect_tx(&pbar[buf], kProjRows * kProjCols * 2);
-            tc::tma_load_2d(wdst, tmap, tw_local, j0, &pbar[buf]);
-          }
-        } else
-        for (int i = ctid; i < rows * pieces_per_row; i += kConsumers) {
-          const int r = i / pieces_per_row, pc = i % pieces_per_row;
-          int which, local;
-          const T* base = col_source<T, D>(p, cb + pc * 8, which, local);
-          const int width = which == 0 ? p.Hq * D : p.Hkv * D;
-          cp_async16(wdst + r * kProjCols + pc * 8, base + (size_t)(j0 + r) * width + local, 16);
-        }
-        T* xdst = xbuf + buf * B * kProjRows;
-        const int xpieces = rows / 8;
-        for (int i = ctid; i < B * xpieces; i += kConsumers) {
-          const int b = i / xpieces, pc = i % xpieces;
-          cp_async16(xdst + b * kProjRows + pc * 8, x + (size_t)b * H + j0 + pc * 8, 16);
-        }
-        cp_async_commit();
-      };
-
-      for (int c = 0; c < S - 1; ++c) issue(c, (g0 + c) % S);
-      for (int c = 0; c < nchunks; ++c) {
-        // chunk c + S - 1 goes into the slot chunk c - 1 used (every thread
-        // passed the barrier after reading it); chunk c is then complete once
-        // at most S - 1 newer groups are pending
-        issue(c + S - 1, (g0 + c + S - 1) % S);
-        cp_async_wait_stages(S - 1);
-        if (tma && !mbar_wait_bounded(&pbar[(g0 + c) % S], ((g0 + c) / S) & 1, abort_flag)) {
-          if (!*abort_flag) record_timeout(p.status, kSiteFull);
-          *abort_flag = 1;
-        }
-        named_bar_sync(kBarConsumers, kConsumers);
-        if (active) {
-          const int rows = min(kProjRows, H - c * kProjRows);
-          const T* wsrc = wbuf + ((g0 + c) % S) * kProjRows * kProjCols;
-          const T* xs = xbuf + ((g0 + c) % S) * B * kProjRows;
-          const bool two = b0 + 1 < B;
-          // 8 rows per step (rows is a multiple of 16): all loads of a step
-          // are issued before its FMA chains, which stay in row order
+// `rows` rows of one staged chunk into NC chains of one column: chain ci is
+// batch row min(b0 + ci * bstep, B - 1) (chains past the thread's last row
+// repeat a real one and are discarded).  Each step adds one exact product of
+// two 16-bit floats with one fp32 rounding, rows in order.
+template <typename T, int NC>
+__device__ __forceinline__ void proj_rows(float (&acc)[8], const T* wcol, const T* xs, int rows,
+                                          int b0, int bstep, int B) {
+  const T* xr[NC];
+#pragma unroll
+  for (int ci = 0; ci < NC; ++ci) xr[ci] = xs + min(b0 + ci * bstep, B - 1) * kProjRows;
 #pragma unroll 2
-          for (int j = 0; j < rows; j += 8) {
-            uint32_t w8[8];
+  for (int j = 0; j < rows; j += 8) {
+    float w[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              w8[k] = *reinterpret_cast<const uint32_t*>(wsrc + (j + k) * kProjCols + pair * 2);
-            const uint4 xa8 = *reinterpret_cast<const uint4*>(xs + b0 * kProjRows + j);
-            const uint4 xb8 =
-                two ? *reinterpret_cast<const uint4*>(xs + (b0 + 1) * kProjRows + j) : xa8;
-            const uint32_t xa4[4] = {xa8.x, xa8.y, xa8.z, xa8.w};
-            const uint32_t xb4[4] = {xb8.x, xb8.y, xb8.z, xb8.w};
+    for (int k = 0; k < 8; ++k) w[k] = DT<T>::to_f(wcol[(j + k) * kProjBlk]);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const float2 w = DT<T>::to_f2(w8[k]);
-              const float2 xa = DT<T>::to_f2(xa4[k / 2]);
-              const float xav = (k & 1) ? xa.y : xa.x;
-              acc[0] = fmaf(xav, w.x, acc[0]);
-              acc[1] = fmaf(xav, w.y, acc[1]);
-              if (two) {
-                const float2 xb = DT<T>::to_f2(xb4[k / 2]);
-                const float xbv = (k & 1) ? xb.y : xb.x;
-                acc[2] = fmaf(xbv, w.x, acc[2]);
-                acc[3] = fmaf(xbv, w.y, acc[3]);
-              }
-            }
-          }
-        }
-        named_bar_sync(kBarConsumers, kConsumers);
-      }
-      if (tma) gdone += nchunks;
-      if (active) {
-        const int col = cb + pair * 2;
-        int which, local;
-        (void)col_source<T, D>(p, col, which, local);
-        for (int bb = 0; bb < 2; ++bb) {
-          const int b = b0 + bb;
-          if (b >= B) break;
-          if (which == 0) {
-            T* q = static_cast<T*>(p.q_ws) + (size_t)b * p.Hq * D + local;
-            q[0] = DT<T>::from_f(acc[bb * 2]);
-            q[1] = DT<T>::from_f(acc[bb * 2 + 1]);
-          } else {
-            const int kvh = local / D, d = local % D;
-            C* ws = static_cast<C*>(p.kv_ws) + ((size_t)b * 2 + (which - 1)) * p.Hkv * D + local;
-            store_pair<T, C>(ws, acc[bb * 2], acc[bb * 2 + 1]);
-            C* host = static_cast<C*>(which == 1 ? p.k_host : p.v_host) +
-                      p.lay.row(b, kvh, seq_len(p, b), D) + d;
-            store_pair<T, C>(host, acc[bb * 2], acc[bb * 2 + 1]);  // the append, across the link
-          }
-        }
+    for (int ci = 0; ci < NC; ++ci) {
+      const uint4 x8 = *reinterpret_cast<const uint4*>(xr[ci] + j);
+      const uint32_t xw[4] = {x8.x, x8.y, x8.z, x8.w};
+#pragma unroll
+      for (int k = 0; k < 8; k += 2) {
+        const float2 xf = DT<T>::to_f2(xw[k / 2]);
+        acc[ci] = fmaf(xf.x, w[k], acc[ci]);
+        acc[ci] = fmaf(xf.y, w[k + 1], acc[ci]);
       }
     }
   }
+}
+
+// Phase A: this CTA's share of the [Wq | Wk | Wv] columns for all B
+// sequences.  The columns go out in 32-column blocks, block i to CTA
+// i mod grid; a CTA projects up to proj_group_max(B) of its blocks per pass.
+// Every output is one fp32 FMA chain over j = 0..H-1 in order, rounded once
+// to T (q) or to the cache element (the fresh k/v, also appended to the host
+// cache).  One thread owns one column and the batch rows b0, b0 + bstep, ...
+// Thread 0 keeps the TMA loads of the weight blocks and of x's columns
+// proj_stages chunks ahead; every consumer warp releases a stage once it has
+// read it.  Chunks are numbered across passes, so the loads run on over a
+// pass boundary.
+template <typename T, typename C, int D>
+__device__ void project_phase(const DecodeParams& p, uint8_t* smem, const DecodeSmem& L, int ctid,
+                              const CUtensorMap* mq, const CUtensorMap* mk, const CUtensorMap* mv,
+                              const CUtensorMap* mx, volatile int* abort_flag) {
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.pbar);
+  uint64_t* empty = full + 4;
+  const int S = L.proj_stages;
+  const int B = p.B, H = p.H;
+  const int nblk = (p.Hq + 2 * p.Hkv) * D / kProjBlk;
+  const int mine = (int)blockIdx.x < nblk ? (nblk - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  if (mine == 0) return;
+  const int gmax = proj_group_max(B);
+  const int nch = (H + kProjRows - 1) / kProjRows;
+  const int total = ((mine + gmax - 1) / gmax) * nch;
+  const int wbytes = kProjRows * kProjBlk * 2;
+  const int lane = ctid % 32;
+
+  auto issue = [&](int it) {  // thread 0: chunk it into stage it mod S
+    const int ps = it / nch, c = it % nch, st = it % S;
+    uint8_t* dst = smem + L.proj + st * L.pstage;
+    const int kb0 = ps * gmax, nb = min(mine - kb0, gmax);
+    tc::fence_proxy_async_smem();
+    tc::mbar_expect_tx(&full[st], nb * wbytes + B * kProjRows * 2);
+    for (int k = 0; k < nb; ++k) {
+      int which, local;
+      (void)col_source<T, D>(p, ((int)blockIdx.x + (kb0 + k) * (int)gridDim.x) * kProjBlk, which,
+                             local);
+      tc::tma_load_2d(dst + k * wbytes, which == 0 ? mq : (which == 1 ? mk : mv), local,
+                      c * kProjRows, &full[st]);
+    }
+    tc::tma_load_2d(dst + gmax * wbytes, mx, c * kProjRows, 0, &full[st]);
+  };
+  int issued = 0, landed = 0;  // thread 0's count of chunks issued / seen complete
+  if (ctid == 0)
+    for (; issued < min(S, total); ++issued) issue(issued);
+
+  float acc[8];
+  for (int it = 0; it < total; ++it) {
+    const int ps = it / nch, c = it % nch, st = it % S;
+    const uint32_t ph = (it / S) & 1;
+    const int kb0 = ps * gmax, nb = min(mine - kb0, gmax);
+    const int ncc = nb * kProjBlk;                 // columns of this pass
+    const int bstep = kConsumers / ncc;            // thread rows
+    const int col = ctid % ncc, b0 = ctid / ncc;   // warp-uniform b0
+    const bool active = b0 < bstep && b0 < B;
+    const int nc = active ? (B - b0 + bstep - 1) / bstep : 0;  // chains of this thread
+    const int ncmax = (B + bstep - 1) / bstep;                 // ... of the busiest thread
+    if (c == 0) {
+#pragma unroll
+      for (int ci = 0; ci < 8; ++ci) acc[ci] = 0.f;
+    }
+    // (warp-uniform decisions: the lanes of a warp leave the loop together)
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[st], ph, abort_flag))) {
+      if (lane == 0) {
+        if (!*abort_flag) record_timeout(p.status, kSiteFull);
+        *abort_flag = 1;
+      }
+      break;
+    }
+    landed = it + 1;
+    if (active) {
+      const uint8_t* stage = smem + L.proj + st * L.pstage;
+      const T* wcol = reinterpret_cast<const T*>(stage + (col / kProjBlk) * wbytes) + col % kProjBlk;
+      const T* xs = reinterpret_cast<const T*>(stage + gmax * wbytes);
+      const int rows = min(kProjRows, H - c * kProjRows);  // a multiple of 16
+      if (ncmax <= 1) proj_rows<T, 1>(acc, wcol, xs, rows, b0, bstep, B);
+      else if (ncmax <= 2) proj_rows<T, 2>(acc, wcol, xs, rows, b0, bstep, B);
+      else if (ncmax <= 4) proj_rows<T, 4>(acc, wcol, xs, rows, b0, bstep, B);
+      else proj_rows<T, 8>(acc, wcol, xs, rows, b0, bstep, B);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+    if (c == nch - 1 && active) {
+      int which, local;
+      (void)col_source<T, D>(p, ((int)blockIdx.x + (kb0 + col / kProjBlk) * (int)gridDim.x) *
+                                        kProjBlk + col % kProjBlk,
+                             which, local);
+#pragma unroll
+      for (int ci = 0; ci < 8; ++ci) {
+        if (ci >= nc) break;
+        const int b = b0 + ci * bstep;
+        if (which == 0) {
+          static_cast<T*>(p.q_ws)[(size_t)b * p.Hq * D + local] = DT<T>::from_f(acc[ci]);
+        } else {
+          const int kvh = local / D, d = local % D;
+          store_one<T, C>(static_cast<C*>(p.kv_ws) + ((size_t)b * 2 + (which - 1)) * p.Hkv * D +
+                              local,
+                          acc[ci]);
+          C* host = static_cast<C*>(which == 1 ? p.k_host : p.v_host) +
+                    p.lay.row(b, kvh, seq_len(p, b), D) + d;
+          store_one<T, C>(host, acc[ci]);  // the append, across the link
+        }
+      }
+    }
+    if (ctid < 32 && it + S < total) {
+      // thread 0 refills the stage once every warp has read it (its own included)
+      bool ok = true;
+      if (ctid == 0) {
+        ok = mbar_wait_bounded(&empty[st], ph, abort_flag);
+        if (ok) {
+          issue(issued++);
+        } else {
+          if (!*abort_flag) record_timeout(p.status, kSiteEmpty);
+          *abort_flag = 1;
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    }
+  }
+  // after a give-up, the loads already issued land before the CTA moves on
+  // (bounded; nothing is left in flight on the normal path)
+  if (ctid == 0)
+    for (int i = landed; i < issued; ++i) mbar_wait_drain(&full[i % S], (i / S) & 1);
 }
 
 struct UnitRange {
@@ -307,7 +325,8 @@ __device__ __forceinline__ UnitRange unit_range(const DecodeParams& p, int u) {
 template <typename T, typename C, int D, int G>
 __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(
     const __grid_constant__ CUtensorMap map_wq, const __grid_constant__ CUtensorMap map_wk,
-    const __grid_constant__ CUtensorMap map_wv, const DecodeParams p) {
+    const __grid_constant__ CUtensorMap map_wv, const __grid_constant__ CUtensorMap map_x,
+    const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int EB = KVE<T, C>::EB;
   constexpr int RB = D * EB;   // bytes per cache row
@@ -327,11 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(
     }
     *abort_flag = 0;
     uint64_t* pb = reinterpret_cast<uint64_t*>(smem + L.pbar);
-    for (int s = 0; s < 8; ++s) mbar_init(&pb[s], 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&pb[s], 1);                    // projection stage s loaded
+      mbar_init(&pb[4 + s], kConsumerWarps);  // ... and read by every consumer warp
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  uint32_t gdone = 0;
 
   const int nunits = p.B * p.Hkv * p.splits;
   constexpr int CPR = RB / 16;  // 16-byte chunks per row
@@ -386,28 +407,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(
   const int ctid = tid;
   const int warp = ctid / 32, lane = ctid % 32;
 
-  // Phase A: projection slice of this CTA.  Columns go out in blocks of
-  // kProjCols (whole 128-byte lines of every weight row) when there are enough
-  // blocks to occupy at least half of the CTAs; narrower projections spread
-  // 8-column bands over every CTA instead.  (Narrow strided pieces of each
-  // row made the weight loads, not the FMA chains, phase A's pace.)
-  if (p.mode != kDecodeAttendOnly) {
-    const int ncol = (p.Hq + 2 * p.Hkv) * D;
-    const int nwide = (ncol + kProjCols - 1) / kProjCols;
-    if (2 * nwide >= (int)gridDim.x) {
-      for (int bi = blockIdx.x; bi < nwide; bi += gridDim.x)
-        project_columns<T, C, D>(p, bi * kProjCols, min(ncol, (bi + 1) * kProjCols), smem, L,
-                                 ctid, &map_wq, &map_wk, &map_wv, gdone, abort_flag);
-    } else {
-      const int nblk = ncol / 8;
-      const int per = nblk / gridDim.x, rem = nblk % gridDim.x;
-      const int b0 = blockIdx.x * per + min((int)blockIdx.x, rem);
-      const int b1 = b0 + per + ((int)blockIdx.x < rem ? 1 : 0);
-      if (b1 > b0)
-        project_columns<T, C, D>(p, b0 * 8, b1 * 8, smem, L, ctid, &map_wq, &map_wk, &map_wv,
-                                 gdone, abort_flag);
-    }
-  }
+  // Phase A: this CTA's projection blocks.
+  if (p.mode != kDecodeAttendOnly)
+    project_phase<T, C, D>(p, smem, L, ctid, &map_wq, &map_wk, &map_wv, &map_x, abort_flag);
   if (p.mode == kDecodeProjectOnly) return;  // the producers returned at once
   if (p.mode == kDecodeFused) {
     // Grid barrier: every CTA's q and fresh k/v are in the workspace.  (The
@@ -636,20 +638,19 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, int smem, cudaStrea
   auto kern = decode_fused_kernel<T, C, D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  // tensor maps for the projection's weight chunks, only where phase A hands
-  // out whole 64-column blocks (the kernel makes the same choice)
-  CUtensorMap mq, mk, mv;
+  // tensor maps for phase A's TMA loads: 32-column x 128-row weight blocks
+  // and x's 128 columns of every sequence (x is [B, H])
+  CUtensorMap mq, mk, mv, mx;
   memset(&mq, 0, sizeof mq);
   memset(&mk, 0, sizeof mk);
   memset(&mv, 0, sizeof mv);
-  DecodeParams pl = p;
-  const int ncol = (p.Hq + 2 * p.Hkv) * D;
-  pl.proj_tma = 2 * ((ncol + kProjCols - 1) / kProjCols) >= grid;
+  memset(&mx, 0, sizeof mx);
   const int dt = std::is_same<T, __nv_bfloat16>::value ? DKV_BF16 : DKV_FP16;
-  if (pl.proj_tma &&
-      (!make_tmap_2d_plain(&mq, p.wq, dt, p.H, (uint64_t)p.Hq * D, kProjCols, kProjRows) ||
-       !make_tmap_2d_plain(&mk, p.wk, dt, p.H, (uint64_t)p.Hkv * D, kProjCols, kProjRows) ||
-       !make_tmap_2d_plain(&mv, p.wv, dt, p.H, (uint64_t)p.Hkv * D, kProjCols, kProjRows)))
+  if (p.mode != kDecodeAttendOnly &&
+      (!make_tmap_2d_plain(&mq, p.wq, dt, p.H, (uint64_t)p.Hq * D, kProjBlk, kProjRows) ||
+       !make_tmap_2d_plain(&mk, p.wk, dt, p.H, (uint64_t)p.Hkv * D, kProjBlk, kProjRows) ||
+       !make_tmap_2d_plain(&mv, p.wv, dt, p.H, (uint64_t)p.Hkv * D, kProjBlk, kProjRows) ||
+       !make_tmap_2d_plain(&mx, p.x, dt, p.B, p.H, kProjRows, p.B)))
     return cudaErrorInvalidValue;
   timer.before(s);
   if (p.len_dev) {
@@ -664,9 +665,9 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, int smem, cudaStrea
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, pl);
+    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mx, p);
   } else {
-    void* args[] = {&mq, &mk, &mv, &pl};
+    void* args[] = {&mq, &mk, &mv, &mx, const_cast<DecodeParams*>(&p)};
     e = cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(kThreads), args,
                                     (size_t)smem, s);
   }

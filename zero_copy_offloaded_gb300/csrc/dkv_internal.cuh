@@ -118,6 +118,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+// Waits, for at most the wait budget and whatever an abort flag says, for
+// the phase with the given parity: after a give-up, asynchronous copies or
+// MMAs already issued complete before the CTA leaves or frees what they use.
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t deadline = global_timer_ns() + kWaitBudgetNs;
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() > deadline) return;
+}
+
 // 16-byte asynchronous global->shared copy; src_bytes < 16 zero-fills the rest
 // (src_bytes == 0 reads nothing).
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
@@ -235,7 +244,6 @@ struct DecodeParams {
   CacheLayout lay;     // rows of k_read / v_read / k_host / v_host
   int mode;            // DecodeMode
   int kv_fp8;          // caches hold 8-bit E4M3 (bf16 activations)
-  int proj_tma;       // phase A takes whole 64-column weight blocks by TMA (maps encoded)
   // lengths: len_dev (device, [B]) when set, so that a captured graph replays
   // with the lengths of the step it runs; else the by-value copy below
   const int* len_dev;

@@ -136,14 +136,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
   return false;
 }
 
-// Waits, for at most the wait budget and whatever the abort flag says, for
-// the phase with the given parity of a barrier that a TMA load completes.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const uint64_t deadline = global_timer_ns() + kWaitBudgetNs;
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() > deadline) return;
-}
-
 // Warp-uniform bounded wait (tcgen05.ld / st after it need the whole warp).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Bars* bars,
                                           DeviceStatus* st, int site) {
@@ -365,8 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // after a give-up nobody consumes the loads still in flight: let the
         // last one into each buffer land before the CTA leaves (bounded)
         for (int s = 0; s < 2; ++s) {
-          if (last_g[s] >= 0) drain_wait(&bars->pr_full[s], (last_g[s] >> 1) & 1);
-          if (last_q[s] >= 0) drain_wait(&bars->q_full[s], (last_q[s] >> 1) & 1);
+          if (last_g[s] >= 0) mbar_wait_drain(&bars->pr_full[s], (last_g[s] >> 1) & 1);
+          if (last_q[s] >= 0) mbar_wait_drain(&bars->q_full[s], (last_q[s] >> 1) & 1);
         }
       }
     }
@@ -469,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (bars->abort) {
         // after a give-up, the MMAs already issued finish before TMEM is freed
         tc::mma_commit(&bars->mma_drain);
-        drain_wait(&bars->mma_drain, 0);
+        mbar_wait_drain(&bars->mma_drain, 0);
       }
     }
     __syncwarp();
