@@ -184,12 +184,16 @@ __device__ __forceinline__ void proj_rows(float (&acc)[8], const T* wcol, const 
 // sequences.  The columns go out in 32-column blocks, block i to CTA
 // i mod grid; a CTA projects up to proj_group_max(B) of its blocks per pass.
 // Every output is one fp32 FMA chain over j = 0..H-1 in order, rounded once
-// to T (q) or to the cache element (the fresh k/v, also appended to the host
-// cache).  One thread owns one column and the batch rows b0, b0 + bstep, ...
+// to T (q) or to the cache element (the fresh k/v; the host append follows
+// the grid-barrier arrival, see append_rows).  Compute slot s, taken by
+// consumer thread (s + 64) mod 256, owns one column and the batch rows
+// b0, b0 + bstep, ...; the rotation puts the first slots on warps 2 and 3,
+// whose sub-partitions no producer warp and not the issuing thread share.
 // Thread 0 keeps the TMA loads of the weight blocks and of x's columns
-// proj_stages chunks ahead; every consumer warp releases a stage once it has
-// read it.  Chunks are numbered across passes, so the loads run on over a
-// pass boundary.
+// proj_stages chunks ahead; each warp with work in a pass releases a stage
+// once it has read it, and thread 0 arrives for the warps without work,
+// which skip the chunk.  Chunks are numbered across passes, so the loads run
+// on over a pass boundary.
 template <typename T, typename C, int D>
 __device__ void project_phase(const DecodeParams& p, uint8_t* smem, const DecodeSmem& L, int ctid,
                               const CUtensorMap* mq, const CUtensorMap* mk, const CUtensorMap* mv,
@@ -206,6 +210,7 @@ __device__ void project_phase(const DecodeParams& p, uint8_t* smem, const Decode
   const int total = ((mine + gmax - 1) / gmax) * nch;
   const int wbytes = kProjRows * kProjBlk * 2;
   const int lane = ctid % 32;
+  const int slot = (ctid + 64) % kConsumers;  // compute slot of this thread
 
   auto issue = [&](int it) {  // thread 0: chunk it into stage it mod S
     const int ps = it / nch, c = it % nch, st = it % S;
@@ -222,9 +227,25 @@ __device__ void project_phase(const DecodeParams& p, uint8_t* smem, const Decode
     }
     tc::tma_load_2d(dst + gmax * wbytes, mx, c * kProjRows, 0, &full[st]);
   };
-  int issued = 0, landed = 0;  // thread 0's count of chunks issued / seen complete
+  int issued = 0, landed = 0;  // thread 0's count of chunks issued / known landed
   if (ctid == 0)
     for (; issued < min(S, total); ++issued) issue(issued);
+  // warp 0: thread 0 refills chunk it's stage with chunk it + S once every warp
+  // has read it; false (for the whole warp) after a give-up
+  auto refill = [&](int it) -> bool {
+    bool ok = true;
+    if (ctid == 0) {
+      ok = mbar_wait_bounded(&empty[it % S], (it / S) & 1, abort_flag);
+      if (ok) {
+        landed = max(landed, it + 1);  // chunk it was read, so it had landed
+        issue(issued++);
+      } else {
+        if (!*abort_flag) record_timeout(p.status, kSiteEmpty);
+        *abort_flag = 1;
+      }
+    }
+    return __shfl_sync(0xffffffffu, ok, 0);
+  };
 
   float acc[8];
   for (int it = 0; it < total; ++it) {
@@ -233,13 +254,22 @@ __device__ void project_phase(const DecodeParams& p, uint8_t* smem, const Decode
     const int kb0 = ps * gmax, nb = min(mine - kb0, gmax);
     const int ncc = nb * kProjBlk;                 // columns of this pass
     const int bstep = kConsumers / ncc;            // thread rows
-    const int col = ctid % ncc, b0 = ctid / ncc;   // warp-uniform b0
+    const int col = slot % ncc, b0 = slot / ncc;   // warp-uniform b0
     const bool active = b0 < bstep && b0 < B;
     const int nc = active ? (B - b0 + bstep - 1) / bstep : 0;  // chains of this thread
     const int ncmax = (B + bstep - 1) / bstep;                 // ... of the busiest thread
+    const int nslots = ncc * min(bstep, B);        // active slots: 0 .. nslots-1
+    const int nwarps = (nslots + 31) / 32;         // warps with work in this pass
+    const bool wact = slot / 32 < nwarps;          // this warp has work
     if (c == 0) {
 #pragma unroll
       for (int ci = 0; ci < 8; ++ci) acc[ci] = 0.f;
+    }
+    if (ctid == 0 && nwarps < kConsumerWarps)
+      mbar_arrive_cnt(&empty[st], kConsumerWarps - nwarps);  // for the warps without work
+    if (!wact) {
+      if (ctid < 32 && it + S < total && !refill(it)) break;  // warp 0 still refills
+      continue;
     }
     // (warp-uniform decisions: the lanes of a warp leave the loop together)
     if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[st], ph, abort_flag))) {
@@ -271,38 +301,45 @@ __device__ void project_phase(const DecodeParams& p, uint8_t* smem, const Decode
       for (int ci = 0; ci < 8; ++ci) {
         if (ci >= nc) break;
         const int b = b0 + ci * bstep;
-        if (which == 0) {
+        if (which == 0)
           static_cast<T*>(p.q_ws)[(size_t)b * p.Hq * D + local] = DT<T>::from_f(acc[ci]);
-        } else {
-          const int kvh = local / D, d = local % D;
+        else
           store_one<T, C>(static_cast<C*>(p.kv_ws) + ((size_t)b * 2 + (which - 1)) * p.Hkv * D +
                               local,
                           acc[ci]);
-          C* host = static_cast<C*>(which == 1 ? p.k_host : p.v_host) +
-                    p.lay.row(b, kvh, seq_len(p, b), D) + d;
-          store_one<T, C>(host, acc[ci]);  // the append, across the link
-        }
       }
     }
-    if (ctid < 32 && it + S < total) {
-      // thread 0 refills the stage once every warp has read it (its own included)
-      bool ok = true;
-      if (ctid == 0) {
-        ok = mbar_wait_bounded(&empty[st], ph, abort_flag);
-        if (ok) {
-          issue(issued++);
-        } else {
-          if (!*abort_flag) record_timeout(p.status, kSiteEmpty);
-          *abort_flag = 1;
-        }
-      }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-    }
+    if (ctid < 32 && it + S < total && !refill(it)) break;
   }
   // after a give-up, the loads already issued land before the CTA moves on
-  // (bounded; nothing is left in flight on the normal path)
-  if (ctid == 0)
+  // (bounded).  Chunks [landed, issued) are at most S consecutive ones, one per
+  // stage, each the stage's latest use, so each parity names its own phase.
+  if (ctid == 0 && *abort_flag)
     for (int i = landed; i < issued; ++i) mbar_wait_drain(&full[i % S], (i / S) & 1);
+}
+
+// The append: the fresh k/v of this CTA's projection blocks, copied from the
+// workspace to the new row of the host cache, 16 bytes at a time (a block's
+// 32 columns are contiguous in both).  The fused kernel runs it after its
+// grid-barrier arrival, so the fence before that arrival does not wait for
+// writes across the link.
+template <typename T, typename C, int D>
+__device__ void append_rows(const DecodeParams& p, int ctid) {
+  constexpr int CB = kProjBlk * (int)sizeof(C) / 16;  // 16-byte pieces per block row
+  const int nq = p.Hq * D, nkv = p.Hkv * D;
+  const int nblk = (p.Hq + 2 * p.Hkv) * D / kProjBlk;
+  const int mine = (int)blockIdx.x < nblk ? (nblk - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  for (int i = ctid; i < mine * p.B * CB; i += kConsumers) {
+    const int piece = i % CB, b = (i / CB) % p.B, k = i / (CB * p.B);
+    const int col0 = ((int)blockIdx.x + k * (int)gridDim.x) * kProjBlk;
+    if (col0 < nq) continue;  // a q block
+    const int which = col0 < nq + nkv ? 0 : 1;  // k or v
+    const int local = col0 - nq - which * nkv;
+    const C* src = static_cast<const C*>(p.kv_ws) + ((size_t)b * 2 + which) * nkv + local;
+    C* dst = static_cast<C*>(which == 0 ? p.k_host : p.v_host) +
+             p.lay.row(b, local / D, seq_len(p, b), D) + local % D;
+    reinterpret_cast<uint4*>(dst)[piece] = __ldcg(reinterpret_cast<const uint4*>(src) + piece);
+  }
 }
 
 struct UnitRange {
@@ -339,6 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(
   uint64_t* empty = full + stages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flag);
 
+  griddep_launch_dependents();  // (no-op unless launched as a programmatic primary)
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full[s], kProducers);
@@ -372,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(
       for (int t = r.t_lo; t < r.t_hi; ++t, ++it) {
         const int stage = it % stages;
         const uint32_t par = ((it / stages) & 1) ^ 1;
-        if (!mbar_wait_bounded(&empty[stage], par, abort_flag)) {
+        if (!mbar_wait_bounded_sleep(&empty[stage], par, abort_flag, 256)) {
           if (!*abort_flag) record_timeout(p.status, kSiteEmpty);
           *abort_flag = 1;
           cp_async_wait_all();
@@ -407,10 +445,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(
   const int ctid = tid;
   const int warp = ctid / 32, lane = ctid % 32;
 
+  // Under a programmatic dependent launch the producers stream the cached rows
+  // (written by earlier steps) at once; x, the workspace and the barrier
+  // counter belong to earlier kernels until they have finished.
+  griddep_wait();
   // Phase A: this CTA's projection blocks.
   if (p.mode != kDecodeAttendOnly)
     project_phase<T, C, D>(p, smem, L, ctid, &map_wq, &map_wk, &map_wv, &map_x, abort_flag);
-  if (p.mode == kDecodeProjectOnly) return;  // the producers returned at once
+  if (p.mode == kDecodeProjectOnly) {  // (the producers returned at once)
+    named_bar_sync(kBarConsumers, kConsumers);
+    if (!*abort_flag) append_rows<T, C, D>(p, ctid);
+    return;
+  }
   if (p.mode == kDecodeFused) {
     // Grid barrier: every CTA's q and fresh k/v are in the workspace.  (The
     // attention-only launch follows the projection launch on the stream.)
@@ -418,6 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(
     if (ctid == 0) {
       __threadfence();
       atomicAdd(&p.status->grid_arrive, 1u);
+    }
+    if (!*abort_flag) append_rows<T, C, D>(p, ctid);
+    if (ctid == 0) {
       const uint64_t deadline = global_timer_ns() + kWaitBudgetNs;
       while (ld_acquire_gpu(&p.status->grid_arrive) < gridDim.x) {
         if (global_timer_ns() > deadline) {
@@ -611,6 +660,10 @@ template <typename T>
 __global__ void decode_combine_kernel(const float* __restrict__ part_o,
                                       const float* __restrict__ part_lse, T* __restrict__ out,
                                       int splits, int D, DeviceStatus* status) {
+  // (launched as a programmatic dependent inside a captured step: the next
+  // kernel may launch now; this one reads nothing before the fused kernel ends)
+  griddep_launch_dependents();
+  griddep_wait();
   const int bh = blockIdx.x;
   if (*(volatile int*)&status->code != 0) {
     for (int d = threadIdx.x; d < D; d += blockDim.x) out[(size_t)bh * D + d] = DT<T>::from_f(NAN);
@@ -660,11 +713,16 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, int smem, cudaStrea
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    // Programmatic dependent launch: the next layer's kernel may start on the
+    // SMs this one leaves and stream its host tiles; whatever it reads or
+    // writes that earlier kernels touch waits for them (griddepcontrol.wait).
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mx, p);
   } else {
     void* args[] = {&mq, &mk, &mv, &mx, const_cast<DecodeParams*>(&p)};
@@ -674,6 +732,20 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, int smem, cudaStrea
   if (e != cudaSuccess) return e;
   timer.after(s);
   if (p.mode == kDecodeProjectOnly) return cudaSuccess;
+  if (p.len_dev) {  // captured: a programmatic dependent of the fused kernel
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.B * p.Hq);
+    cfg.blockDim = dim3(D);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<T>, (const float*)p.part_o,
+                              (const float*)p.part_lse, static_cast<T*>(p.out), p.splits, D,
+                              p.status);
+  }
   decode_combine_kernel<T><<<p.B * p.Hq, D, 0, s>>>(p.part_o, p.part_lse,
                                                     static_cast<T*>(p.out), p.splits, D,
                                                     p.status);

@@ -79,6 +79,24 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
                : "memory");
 }
 
+// Programmatic dependent launch (no-ops for a kernel launched without it):
+// let the next kernel in the stream launch, and wait until every earlier
+// kernel has finished and its memory operations are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// `count` arrivals at once (count > 0): one thread standing in for several.
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                   smem_u32(bar)),
+               "r"(count)
+               : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -114,6 +132,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   while (!mbar_try_wait(bar, parity)) {
     if (*abort) return false;
     if (global_timer_ns() > deadline) return false;
+  }
+  return true;
+}
+
+// mbar_wait_bounded for waits that are expected to be long (a producer
+// waiting for a free ring slot): between tests the thread sleeps about
+// `ns` nanoseconds, leaving the issue slots to the warps that compute.
+__device__ __forceinline__ bool mbar_wait_bounded_sleep(uint64_t* bar, uint32_t parity,
+                                                        volatile int* abort, unsigned ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t deadline = global_timer_ns() + kWaitBudgetNs;
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (global_timer_ns() > deadline) return false;
+    __nanosleep(ns);
   }
   return true;
 }
