@@ -246,6 +246,17 @@ def bench_decode_config(w, dkv, torch, dev, stream, flush, link_rd, steps, warmu
            "tok_s": w.B / (step_ms * 1e-3), "fused_kernel_ms": kern_ms,
            "host_link_gbs": hb / (kern_ms * 1e-3) / 1e9,
            "frac_of_link": hb / (kern_ms * 1e-3) / 1e9 / link_rd, "clocks": clk}
+    # what launch and completion alone add to an event-timed kernel of the
+    # decode's shape (an empty cooperative kernel, one 320-thread CTA with
+    # 200 KB of shared memory per SM), and the fraction of the link that
+    # a kernel of zero compute time would reach at this cache size
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    floor = statistics.median(_timed_steps(
+        torch, stream, flush, lambda: dkv.dkv_probe_launch(sms, 320, 200 * 1024, stream), 50, 5,
+        min_s=0.0))
+    link_ms = hb / (link_rd * 1e9) * 1e3
+    res["launch_floor_ms"] = floor
+    res["frac_of_link_ceiling"] = link_ms / (link_ms + floor)
     if baselines:
         q = torch.randn((w.B, w.Hq, w.D), device=dev).to(tdt)
         o2 = torch.empty_like(q)

@@ -316,6 +316,14 @@ dkv_status dkv_probe_read(const void* src, size_t bytes, void* sink, void* strea
 /* Write `bytes` (a multiple of 16) of a pattern to `dst` with 16-byte stores. */
 dkv_status dkv_probe_write(void* dst, size_t bytes, void* stream);
 
+/* Launch floor: an empty kernel (it reads and writes nothing) launched
+ * cooperatively with `grid` CTAs of `threads` threads (a multiple of 32, at
+ * most 1024) and `smem_bytes` of dynamic shared memory (at most 227 KB).
+ * Timed with CUDA events around it, it gives what launch and completion add
+ * to a kernel's measured time.  INVALID_ARG for another shape; a grid that
+ * cannot be co-resident is reported as a CUDA error. */
+dkv_status dkv_probe_launch(int grid, int threads, int smem_bytes, void* stream);
+
 /* Naive untiled zero-copy decode attention (the pages' "naive zero-copy"
  * baseline, "Paper Notes: DirectKV", Experiments, CPU-aware tiling): one CTA
  * per (sequence, query head, split) reads its KV head's rows straight from

@@ -71,6 +71,9 @@ def test_invalid_arguments_fail_before_gpu_work(L):
     assert L.dkv_sync_status(None, None) == 1
     assert L.dkv_probe_read(None, 16, None, None) == 1
     assert L.dkv_probe_write(None, 0, None) == 1
+    assert L.dkv_probe_launch(0, 320, 0, None) == 1       # empty grid
+    assert L.dkv_probe_launch(1, 100, 0, None) == 1       # threads not a warp multiple
+    assert L.dkv_probe_launch(1, 320, 300000, None) == 1  # more shared memory than a CTA has
     assert "invalid" in dkv.dkv_last_error()
     # paged caches: page size a power of two, positive pool and table sizes
     assert L.dkv_cache_alloc_paged(ctypes.byref(h), 1, 1, 128, 12, 4, 4, 0) == 1

@@ -21,7 +21,7 @@ __all__ = [
     "dkv_cache_alloc", "dkv_free", "dkv_cache_host_ptrs", "dkv_cache_device_ptrs",
     "dkv_cache_set_lengths", "dkv_cache_get_lengths", "dkv_cache_info", "dkv_cache_reserve",
     "dkv_cache_set_tuning", "dkv_decode", "dkv_prefill", "dkv_sync_status", "dkv_status_str",
-    "dkv_last_error", "dkv_probe_read", "dkv_probe_write", "dkv_attend_naive",
+    "dkv_last_error", "dkv_probe_read", "dkv_probe_write", "dkv_probe_launch", "dkv_attend_naive",
     "dkv_decode_staged", "dkv_prefill_staged", "dkv_prefill_naive", "dkv_decode_unfused", "dkv_last_launch_count", "dkv_cache_kernel_timing",
     "dkv_cache_last_kernel_ms", "dkv_cache_alloc_paged", "dkv_cache_set_page_table",
     "PagedKVCache", "LayeredKVCache", "dkv_cache_alloc_layered", "dkv_decode_layer",
@@ -114,6 +114,7 @@ def lib(build_if_missing: bool = False):
         "dkv_sync_status": [P, P],
         "dkv_probe_read": [P, Z, P, P],
         "dkv_probe_write": [P, Z, P],
+        "dkv_probe_launch": [I, I, I, P],
         "dkv_attend_naive": [P, P, I, P, P],
         "dkv_decode_staged": [P, P, P, P, P, I, I, P, P, P, P],
         "dkv_prefill_staged": [P, P, I, P, P, P, I, I, P, P, P, P],
@@ -339,6 +340,10 @@ def dkv_probe_read(src, nbytes, sink, stream=None):
 
 def dkv_probe_write(dst, nbytes, stream=None):
     _check(lib().dkv_probe_write(_ptr(dst), nbytes, _stream(stream)), "dkv_probe_write")
+
+
+def dkv_probe_launch(grid, threads, smem_bytes, stream=None):
+    _check(lib().dkv_probe_launch(grid, threads, smem_bytes, _stream(stream)), "dkv_probe_launch")
 
 
 def dkv_attend_naive(h, q, n_q_heads, out, stream=None):

@@ -1024,6 +1024,14 @@ dkv_status dkv_probe_write(void* dst, size_t bytes, void* stream) {
   return e == cudaSuccess ? DKV_OK : cuda_fail(e, "probe write launch");
 }
 
+dkv_status dkv_probe_launch(int grid, int threads, int smem_bytes, void* stream) {
+  if (grid < 1 || threads < 32 || threads > 1024 || threads % 32 || smem_bytes < 0 ||
+      smem_bytes > 232448)
+    return fail(DKV_ERR_INVALID_ARG, "invalid launch shape");
+  cudaError_t e = launch_probe_empty(grid, threads, smem_bytes, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DKV_OK : cuda_fail(e, "probe launch");
+}
+
 dkv_status dkv_attend_naive(dkv_cache* c, const void* q, int n_q_heads, void* out, void* stream) {
   if (!valid(c) || !q || !out || n_q_heads <= 0 || n_q_heads % c->Hkv)
     return fail(DKV_ERR_INVALID_ARG, "invalid argument");

@@ -339,6 +339,7 @@ cudaError_t launch_gemm_tc(const void* x, const void* w, void* y, int M, int N, 
 
 cudaError_t launch_probe_read(const void* src, size_t bytes, void* sink, cudaStream_t s);
 cudaError_t launch_probe_write(void* dst, size_t bytes, cudaStream_t s);
+cudaError_t launch_probe_empty(int grid, int threads, int smem, cudaStream_t s);
 cudaError_t launch_attend_naive(const void* q, const void* k, const void* v, void* out,
                                 float* part_o, float* part_lse, int B, int Hq, int Hkv, int D,
                                 int S_max, const int* len, int splits, int dtype, cudaStream_t s);

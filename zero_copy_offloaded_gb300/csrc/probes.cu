@@ -41,6 +41,12 @@ __global__ void __launch_bounds__(kProbeThreads) probe_write_kernel(uint4* __res
     __stcs(dst + i, make_uint4((uint32_t)i, 0x5A5A5A5Au, (uint32_t)(i >> 32), 0xA5A5A5A5u));
 }
 
+// Launch floor: a kernel that does nothing and touches no memory, launched
+// cooperatively with a given grid, block and dynamic shared memory.  Timed
+// with CUDA events like a decode call, it is the part of a kernel's measured
+// time that launch and completion take.
+__global__ void probe_launch_kernel() {}
+
 // Naive zero-copy attention: one CTA per (b, q head, split), 4 warps.  Each
 // lane of a warp scores its own key by reading the key row from the host
 // pointer directly; P.V reads the value rows from the host pointer directly.
@@ -157,6 +163,14 @@ cudaError_t launch_probe_read(const void* src, size_t bytes, void* sink, cudaStr
   probe_read_kernel<<<probe_grid(), kProbeThreads, 0, s>>>(static_cast<const uint4*>(src),
                                                            bytes / 16, static_cast<uint4*>(sink));
   return cudaGetLastError();
+}
+
+cudaError_t launch_probe_empty(int grid, int threads, int smem, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(probe_launch_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchCooperativeKernel((const void*)probe_launch_kernel, dim3(grid), dim3(threads),
+                                     nullptr, (size_t)smem, s);
 }
 
 cudaError_t launch_probe_write(void* dst, size_t bytes, cudaStream_t s) {
