@@ -9,15 +9,18 @@
 // is read once and reused by every query head of its KV group (Key Ideas (1)).
 //
 // GB300 design: one persistent cooperative launch, one CTA per SM.
-//   Phase A  every CTA projects a slice of the [Wq | Wk | Wv] columns for all
-//            sequences (fp32 FMA chain over H in order, rounded once), writes
-//            q and the fresh k/v to a small HBM workspace and appends k/v to
-//            the host cache.  Whole 64-column weight blocks arrive by TMA, so
+//   Phase A  every CTA projects its 32-column blocks of [Wq | Wk | Wv] for all
+//            sequences (one fp32 FMA chain over H in order per output, one
+//            column per thread, rounded once) and writes q and the fresh k/v
+//            to a small HBM workspace.  Weight blocks and x arrive by TMA, so
 //            this HBM traffic stays off the load/store path of the host
 //            requests.  Meanwhile the producer warps already stream the CTA's
 //            first host tiles into the shared-memory ring.
 //   barrier  bounded grid-wide arrival counter (co-residency is guaranteed by
-//            the cooperative launch).
+//            the cooperative launch); after its arrival each CTA copies its
+//            fresh k/v rows from the workspace to the host cache (the append).
+// In a captured step the kernels are programmatic dependents: the producers
+// start at once, everything else waits for the earlier kernels.
 //   Phase B  units (sequence b, KV head, key-range split) in a static
 //            round-robin.  Producer warps copy host K/V tiles with 16-byte
 //            cp.async into an m-stage ring (mbarrier hand-off), one tile in

@@ -176,7 +176,7 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, int dtype, uint64_t rows, 
 }
 
 // The same without swizzle: a box lands as box_rows dense rows of box_cols * 2
-// bytes (the decode projection's 64-column weight chunks).
+// bytes (the decode projection's 32-column weight blocks and x's columns).
 bool make_tmap_2d_plain(CUtensorMap* map, const void* base, int dtype, uint64_t rows,
                         uint64_t cols, uint32_t box_cols, uint32_t box_rows) {
   EncodeFn fn = encode_fn();
