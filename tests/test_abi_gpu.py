@@ -29,3 +29,20 @@ def test_freed_handle_is_refused():
     with pytest.raises(dkv.DkvError) as ei:
         dkv.dkv_decode(h, x, wq, wk, wk, 64, 4, out)
     assert ei.value.name == "DKV_ERR_INVALID_ARG"
+
+
+def test_launch_probe_runs_and_times_an_empty_kernel():
+    """The launch-floor probe launches cooperatively in the decode's shape (one
+    320-thread CTA with 200 KB of shared memory per SM) and in a small shape;
+    its event-timed cost is positive and well under a millisecond."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    s = torch.cuda.current_stream()
+    for grid, smem in ((sms, 200 * 1024), (4, 0)):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dkv.dkv_probe_launch(grid, 320, smem, s)  # warm (function attributes)
+        a.record(s)
+        dkv.dkv_probe_launch(grid, 320, smem, s)
+        b.record(s)
+        b.synchronize()
+        assert 0.0 < a.elapsed_time(b) < 1.0

@@ -135,6 +135,44 @@ def test_captured_step_replays(dtype, D, Hq, Hkv):
         lay.free()
 
 
+def test_captured_steps_back_to_back():
+    """Three captured three-layer steps launched with no synchronisation in
+    between: inside a graph each layer's kernels are programmatic dependents of
+    the previous layer's, and graphs follow one another on the stream.  Every
+    step's appended rows, at their own lengths, and the last step's outputs
+    match the oracle run step by step."""
+    w = wl.Workload("t", "decode", B=2, H=256, Hq=8, Hkv=2, D=128, P=300, seed=43)
+    lay = Layers(3, w, [300, 17], 320)
+    try:
+        outs = [_decode_out(w) for _ in range(lay.L)]
+        xs = [d["x"].reshape(w.B, 1, w.H) for d in lay.dev]
+        lay.cache.capture_step(xs, [d["wq"] for d in lay.dev], [d["wk"] for d in lay.dev],
+                               [d["wv"] for d in lay.dev], w.Hq, outs)
+        lens = lay.lens.copy()
+        for _ in range(3):
+            lay.cache.launch_step()
+        lay.cache.sync()
+        assert list(lay.cache.lengths()) == list(lens + 3)
+        for step in range(3):
+            for l in range(lay.L):
+                ref = lay.oracle(l, lay.dense[l]["x"][:, :1], lay.k0[l], lay.v0[l], lens)
+                kh, vh = lay.cache.k_host[l], lay.cache.v_host[l]
+                for b in range(w.B):
+                    p = int(lens[b])
+                    assert np.array_equal(kh[b, :, p], ref["k_new"][b, 0]), f"step {step} layer {l}"
+                    assert np.array_equal(vh[b, :, p], ref["v_new"][b, 0]), f"step {step} layer {l}"
+                if step == 2:
+                    got = out_f64(outs[l], w.dtype).reshape(w.B, w.Hq, w.D)
+                    assert_close(got, ref["out"].reshape(w.B, w.Hq, w.D), f"last step layer {l}")
+                lay.k0[l], lay.v0[l] = ref["k_cache_after"], ref["v_cache_after"]
+            lens = lens + 1
+        for l in range(lay.L):  # nothing written past the last step's rows
+            for b in range(w.B):
+                assert np.all(lay.cache.k_host[l][b, :, int(lens[b]):] == 0x7E57)
+    finally:
+        lay.free()
+
+
 def test_layered_prefill_then_captured_decode():
     w = wl.Workload("t", "prefill", B=2, H=128, Hq=8, Hkv=2, D=128, P=100, T=60, seed=51)
     lay = Layers(2, w, [100, 30], 200)
