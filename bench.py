@@ -464,6 +464,31 @@ def oracle_decode_sample(w: wl.Workload, seqs: int = 1, threads: int = 0):
     return dt, oracle.max_threads()
 
 
+def oracle_prefill_sample(w: wl.Workload, nrows: int = 512, threads: int = 0):
+    """Time the fp64 oracle on the prefill workload with a seeded subset of
+    query rows (the first and last token of sequence 0 among them): the whole
+    projection (every new K/V row is a key of some sampled row), then attention
+    of the sampled rows over all heads.  Returns (seconds, threads, algorithmic
+    FLOPs of that work, sample description)."""
+    import oracle
+    oracle.set_threads(threads or host_cores())
+    d = wl.make_dense(w)
+    k = np.zeros((w.B, w.Hkv, w.S_max, w.D), np.uint16)
+    v = np.zeros_like(k)
+    wl.fill_cache(w, k, v)
+    rng = np.random.default_rng(0)
+    ts = sorted({0, w.T - 1} | set(int(t) for t in rng.choice(w.T, nrows - 2, replace=False)))
+    rows = [(0, t) for t in ts]
+    oracle.lib()
+    t0 = time.perf_counter()
+    oracle.step(d["x"], d["wq"], d["wk"], d["wv"], k, v, w.P, w.Hq, w.dtype, rows=rows)
+    dt = time.perf_counter() - t0
+    flops = w.proj_flops() + sum(4 * w.Hq * w.D * (w.P + t + 1) for _, t in rows)
+    sample = (f"{w.name}: the whole projection ({w.B * w.T} tokens) and {len(rows)} seeded "
+              f"query rows of sequence 0 (all {w.Hq} heads)")
+    return dt, oracle.max_threads(), flops, sample
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -726,6 +751,10 @@ def main():
         t_all, _ = min(oracle_decode_sample(tw) for _ in range(3))
         t_one, _ = min(oracle_decode_sample(tw, threads=1) for _ in range(3))
         cpu["tiny_decode"] = {"tok_s_all_cores": 1.0 / t_all, "tok_s_one_core": 1.0 / t_one}
+        # and on the prefill workload, a bounded sample in the prefill's unit
+        pdt, pcores, pflops, psample = oracle_prefill_sample(wl.WORKLOADS[args.prefill_workload])
+        cpu["prefill"] = {"value": pflops / pdt / 1e12, "unit": "TFLOP/s", "cores": pcores,
+                          "kind": "oracle", "seconds": pdt, "sample": psample}
 
     if rank == 0:
         line = {
