@@ -477,7 +477,8 @@ def oracle_prefill_sample(w: wl.Workload, nrows: int = 512, threads: int = 0):
     v = np.zeros_like(k)
     wl.fill_cache(w, k, v)
     rng = np.random.default_rng(0)
-    ts = sorted({0, w.T - 1} | set(int(t) for t in rng.choice(w.T, nrows - 2, replace=False)))
+    extra = max(0, min(nrows, w.T) - 2)
+    ts = sorted({0, w.T - 1} | set(int(t) for t in rng.choice(w.T, extra, replace=False)))
     rows = [(0, t) for t in ts]
     oracle.lib()
     t0 = time.perf_counter()
