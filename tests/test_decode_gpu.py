@@ -170,6 +170,23 @@ def test_decode_longctx_spiked():
         case.free()
 
 
+@pytest.mark.parametrize("B,H,D", [(31, 208, 128), (33, 128, 128), (40, 64, 128), (3, 208, 64)])
+def test_decode_projection_batch_edges(B, H, D):
+    """The projection's batch mapping at its edges: two weight blocks per pass
+    up to 32 sequences (31: up to eight chains a thread), one block per pass
+    beyond (33, 40), and a hidden size whose last 128-row chunk is partial
+    (208 = 128 + 80); appends bit-exact, outputs within the bars."""
+    w = wl.Workload("t", "decode", B=B, H=H, Hq=8, Hkv=2, D=D, P=70, seed=B + H)
+    lens = [(11 * b + 3) % 71 for b in range(B)]
+    case = Case(w, lens=lens, s_max=80)
+    try:
+        out = case.run_decode()
+        check_decode(case, out, case.oracle(), f"B={B} H={H} D={D}")
+        assert list(case.cache.lengths()) == [n + 1 for n in lens]
+    finally:
+        case.free()
+
+
 def test_decode_max_batch():
     """The largest batch a call takes (64 sequences), ragged lengths including 0."""
     w = wl.Workload("t", "decode", B=64, H=128, Hq=8, Hkv=2, D=64, P=200, seed=64)
