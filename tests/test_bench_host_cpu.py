@@ -41,3 +41,22 @@ def test_traffic_reported_only_for_the_sources_it_was_taken_on(monkeypatch):
     monkeypatch.setattr(bench, "kernel_source_hash", lambda fs: "0" * 16)
     assert bench.ncu_traffic(key, files) is None
     assert bench.ncu_traffic("no_such_kernel/none", files) is None
+
+
+def test_oracle_prefill_sample_counts_its_work():
+    """The CPU-baseline sample of the prefill: a positive time, the thread
+    count it ran on, and FLOPs = the whole projection plus the attention of
+    the sampled rows (first and last token included), each row over all heads."""
+    from zero_copy_offloaded_gb300 import workloads as wl
+    w = wl.Workload("t", "prefill", B=1, H=64, Hq=4, Hkv=2, D=16, P=40, T=12, seed=3)
+    dt, cores, flops, sample = bench.oracle_prefill_sample(w, nrows=5)
+    assert dt > 0 and cores >= 1
+    attn = flops - w.proj_flops()
+    per_key = 4 * w.Hq * w.D
+    assert attn % per_key == 0
+    keys = attn // per_key  # sum over the sampled rows t of P + t + 1
+    # five distinct rows among 0..T-1, the first and last included
+    lo = (w.P + 1) + (w.P + w.T) + sum(w.P + 1 + t for t in range(1, 4))
+    hi = (w.P + 1) + (w.P + w.T) + sum(w.P + 1 + t for t in range(w.T - 4, w.T - 1))
+    assert lo <= keys <= hi
+    assert "5 seeded query rows" in sample
