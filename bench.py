@@ -838,19 +838,26 @@ def bench_prefill(args, dkv, torch, dev, stream, flush, pk, link_rd, link_wr, hb
     out = torch.empty((w.B, w.T, w.Hq, w.D), dtype=tdt, device=dev)
     lens = np.full(w.B, w.P, np.int32)
     dkv.dkv_cache_reserve(cache.h, w.Hq, w.T)
-    dkv.dkv_cache_kernel_timing(cache.h, True)
-    kern = []
 
     def call():
         cache.set_lengths(lens)
         cache.prefill(x, wq, wk, wv, w.Hq, out, stream)
-        kern.append(dkv.dkv_cache_last_kernel_ms(cache.h))
+    # whole calls without the library's per-kernel events, which would sit
+    # between the launches and keep them from overlapping
+    dkv.dkv_cache_kernel_timing(cache.h, False)
     clocks = Clocks(clock_index) if clock_index is not None else None
     if clocks:
         clocks.start()
     times = _timed_steps(torch, stream, flush, call, max(args.steps, 10), args.warmup)
     clk = clocks.stop() if clocks else None
-    kern = kern[max(args.warmup, 3):]
+    cache.sync(stream)
+    # then the fused kernel's own time, from calls with those events on
+    dkv.dkv_cache_kernel_timing(cache.h, True)
+    kern = []
+    for _ in range(max(args.steps, 10)):
+        _time_once(torch, stream, flush, call)
+        kern.append(dkv.dkv_cache_last_kernel_ms(cache.h))
+    dkv.dkv_cache_kernel_timing(cache.h, False)
     cache.sync(stream)
 
     def naive():
