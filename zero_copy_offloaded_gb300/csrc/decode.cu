@@ -57,18 +57,6 @@ struct KVE<T, __nv_fp8_e4m3> {
   }
 };
 
-// The two fp32 sums of a column pair stored as cache elements (rounded once).
-template <typename T, typename C>
-__device__ __forceinline__ void store_pair(C* dst, float a, float b) {
-  if constexpr (KVE<T, C>::EB == 1) {
-    *reinterpret_cast<__nv_fp8x2_storage_t*>(dst) =
-        __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-  } else {
-    dst[0] = DT<T>::from_f(a);
-    dst[1] = DT<T>::from_f(b);
-  }
-}
-
 // 16-byte chunk c of cache row n at chunk c ^ (n mod m), m = min(chunks per
 // row, 8): rows read at the same column hit different bank groups.
 template <int CPR>
