@@ -60,6 +60,9 @@ constexpr uint32_t kTmO = 128;
 
 template <int D>
 struct TcCfg {
+  // projection staging stages: four where shared memory has room (D = 64,
+  // 192 KB), two at D = 128 (they fill the Q buffers and the output staging)
+  static constexpr int SP = D == 64 ? 4 : 2;
   static constexpr int DR = D / 64;                    // 128-byte regions per row
   static constexpr int kKV = DR * kRegKV;              // one of K or V
   static constexpr int kQ = DR * kRegQ;                // one Q tile
@@ -68,13 +71,13 @@ struct TcCfg {
   static constexpr int kOffV = kOffK + kKV;
   static constexpr int kOffQ = kOffV + kKV;            // two Q buffers
   static constexpr int kOffO = kOffQ + 2 * kQ;
-  // projection staging (aliases the Q buffers and the output staging): x block
-  // [128 x 64] and W block [64 x 2D], two stages
+  // projection staging (aliases the Q buffers, the output staging and what
+  // follows): x block [128 x 64] and W block [64 x 2D], SP stages
   static constexpr int kProjA = kBQ * 64 * 2;          // 16 KB
   static constexpr int kProjB = 64 * 2 * D * 2;        // 16 / 32 KB
   static constexpr int kProjStage = kProjA + kProjB;
-  static constexpr int kEnd = (kOffO + kO) > (kOffQ + 2 * kProjStage) ? (kOffO + kO)
-                                                                       : (kOffQ + 2 * kProjStage);
+  static constexpr int kEnd = (kOffO + kO) > (kOffQ + SP * kProjStage) ? (kOffO + kO)
+                                                                        : (kOffQ + SP * kProjStage);
   static constexpr int kOffBar = kEnd;
 };
 
@@ -89,7 +92,7 @@ constexpr int smem_request() {
 }
 
 struct Bars {
-  uint64_t q_full[2], q_empty[2], kv_host, kv_ready, pr_full[2], pr_empty[2], pr_done, pr_drain;
+  uint64_t q_full[2], q_empty[2], kv_host, kv_ready, pr_full[4], pr_empty[4], pr_done, pr_drain;
   // one phase: every projection pass's MMAs have completed (the loader's
   // signal that the staging it aliases with the Q buffers is free; pr_done
   // has a phase per pass, and a thread outside the pass hand-offs could see
@@ -258,6 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
+    }
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&bars->pr_full[i], 1);
       mbar_init(&bars->pr_empty[i], 1);
     }
@@ -308,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) {
       // last load issued into each projection stage / Q buffer (-1: none)
-      int last_g[2] = {-1, -1}, last_q[2] = {-1, -1};
+      int last_g[4] = {-1, -1, -1, -1}, last_q[2] = {-1, -1};
       tc::prefetch_tmap(&map_q);
       // (b) projection operands, one 128-row pass at a time: x rows, [Wk | Wv]
       if (has_new) {
@@ -319,8 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int xrow = b * a.T + (k0 + (pass0 + ps) * 128 - P);  // may be negative: zeros
           for (int kb = 0; kb < nk_proj; ++kb) {
             const int g = ps * nk_proj + kb;
-            const int s = g & 1;
-            if (!wait_or_abort(&bars->pr_empty[s], ((g >> 1) & 1) ^ 1, bars, a.status, kSiteEmpty))
+            const int s = g % Cfg::SP;
+            if (!wait_or_abort(&bars->pr_empty[s], ((g / Cfg::SP) & 1) ^ 1, bars, a.status,
+                               kSiteEmpty))
               break;
             uint8_t* pa = qs + s * Cfg::kProjStage;
             uint8_t* pb = pa + Cfg::kProjA;
@@ -356,10 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (bars->abort) {
         // after a give-up nobody consumes the loads still in flight: let the
         // last one into each buffer land before the CTA leaves (bounded)
-        for (int s = 0; s < 2; ++s) {
-          if (last_g[s] >= 0) mbar_wait_drain(&bars->pr_full[s], (last_g[s] >> 1) & 1);
+        for (int s = 0; s < Cfg::SP; ++s)
+          if (last_g[s] >= 0) mbar_wait_drain(&bars->pr_full[s], (last_g[s] / Cfg::SP) & 1);
+        for (int s = 0; s < 2; ++s)
           if (last_q[s] >= 0) mbar_wait_drain(&bars->q_full[s], (last_q[s] >> 1) & 1);
-        }
       }
     }
     cp_async_wait_all();
@@ -377,8 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::fence_after_sync();
           for (int kb = 0; kb < nk_proj; ++kb) {
             const int g = ps * nk_proj + kb;
-            const int s = g & 1;
-            if (!wait_or_abort(&bars->pr_full[s], (g >> 1) & 1, bars, a.status, kSiteFull)) break;
+            const int s = g % Cfg::SP;
+            if (!wait_or_abort(&bars->pr_full[s], (g / Cfg::SP) & 1, bars, a.status, kSiteFull))
+              break;
             tc::fence_after_sync();
             const uint32_t pa = smem_u32(qs + s * Cfg::kProjStage);
             const uint32_t pb = pa + Cfg::kProjA;
