@@ -39,15 +39,17 @@ def test_withheld_tile_times_out_then_recovers():
         case.free()
 
 
-def test_withheld_prefill_rows_time_out_then_recover():
-    """The prefill's loader withholds the arrival of its chunk's host rows:
-    the bounded waits give up, DKV_ERR_TIMEOUT is reported, the outputs are
-    NaN (the combine sees the status), the prefix is intact, and the next
-    prefill on the same context is correct."""
+@pytest.mark.parametrize("D", [128, 64])
+def test_withheld_prefill_rows_time_out_then_recover(D):
+    """The prefill withholds the arrival of its chunks' host rows: the bounded
+    waits give up, DKV_ERR_TIMEOUT is reported, the outputs are NaN (the
+    combine sees the status), the prefix is intact, and the next prefill on
+    the same context is correct.  D = 64 stages the new-token projection four
+    deep, D = 128 two deep; both must drain their in-flight loads and give up."""
     import torch
     import zero_copy_offloaded_gb300 as dkv
     from .test_prefill_gpu import check_prefill
-    w = wl.Workload("t", "prefill", B=2, H=128, Hq=8, Hkv=2, D=128, P=600, T=70, seed=37)
+    w = wl.Workload("t", "prefill", B=2, H=128, Hq=8, Hkv=2, D=D, P=600, T=70, seed=37)
     case = Case(w, s_max=w.P + w.T + 3)
     try:
         dkv.dkv_cache_debug_withhold(case.cache.h, True)

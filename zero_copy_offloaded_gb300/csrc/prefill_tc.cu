@@ -11,9 +11,10 @@
 //   1. The chunk's K and V land in shared memory (128-byte swizzled rows):
 //      cached rows with 16-byte cp.async from the mapped host cache (each host
 //      byte crosses the link once), new rows from a tcgen05 GEMM
-//      [x rows] . [Wk | Wv] (TMA-fed, accumulator in TMEM, 128 rows per pass)
-//      whose epilogue rounds them, writes them into the stationary tile and
-//      appends them to the host cache.
+//      [x rows] . [Wk | Wv] (TMA-fed, 128 rows per pass, each pass
+//      accumulating in its own TMEM columns) whose epilogue rounds them,
+//      writes them into the stationary tile and appends them to the host
+//      cache in whole 128-byte lines.
 //   2. Every Q tile of the KV group that can see the chunk (128 rows = 128/G
 //      tokens x G heads, TMA from HBM) runs S = Q.K^T (tcgen05, N = 256, TMEM),
 //      a complete softmax over the chunk (it is stationary, so there is no
@@ -92,12 +93,14 @@ constexpr int smem_request() {
 }
 
 struct Bars {
-  uint64_t q_full[2], q_empty[2], kv_host, kv_ready, pr_full[4], pr_empty[4], pr_done, pr_drain;
-  // one phase: every projection pass's MMAs have completed (the loader's
-  // signal that the staging it aliases with the Q buffers is free; pr_done
-  // has a phase per pass, and a thread outside the pass hand-offs could see
-  // both complete before its first test and then wait on the wrong phase)
-  uint64_t pr_all;
+  uint64_t q_full[2], q_empty[2], kv_host, kv_ready, pr_full[4], pr_empty[4];
+  // one phase each: projection pass p's MMAs have completed (pr_done[p]);
+  // every pass's MMAs have completed (pr_all: the loader's signal that the
+  // staging it aliases with the Q buffers is free)
+  uint64_t pr_done[2], pr_all;
+  // one phase each: the four warps of epilogue half h have written pass p's
+  // rows into the stationary tile (they then append those rows from it)
+  uint64_t ap_sync[2][2];
   // per TMEM region: S computed, P written (4 warps), O computed, O read out
   // (4 warps: the region may take the next tile's S)
   uint64_t s_full[2], p_full[2], o_full[2], r_free[2];
@@ -275,9 +278,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int q = 0; q < 4; ++q) mbar_init(&bars->st_free[q], 1);
     mbar_init(&bars->kv_host, 32);
     mbar_init(&bars->kv_ready, 8);
-    mbar_init(&bars->pr_done, 1);
+    for (int p = 0; p < 2; ++p) {
+      mbar_init(&bars->pr_done[p], 1);
+      mbar_init(&bars->ap_sync[0][p], 4);
+      mbar_init(&bars->ap_sync[1][p], 4);
+    }
     mbar_init(&bars->pr_all, 1);
-    mbar_init(&bars->pr_drain, 8);
     mbar_init(&bars->vsync, 4);
     mbar_init(&bars->mma_drain, 1);
     bars->abort = 0;
@@ -373,14 +379,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================= MMA
     if (lane == 0) {
       const bool bf = DT<T>::code == DKV_BF16;
-      // projection passes: [128 x H] . [H x 2D] -> TMEM columns 0..2D-1
+      // projection passes: [128 x H] . [H x 2D] -> TMEM columns [2D p, 2D p + 2D)
+      // for pass p (2 passes x 2D <= 512 columns), so pass 1 runs while the
+      // epilogue warps read pass 0 out
       if (has_new) {
         const uint32_t idesc = tc::idesc_f16(bf, 128, 2 * D, false, true);
         for (int ps = 0; ps < npass && !bars->abort; ++ps) {
-          if (ps > 0 &&  // the softmax warps have drained the previous pass
-              !wait_or_abort(&bars->pr_drain, (ps - 1) & 1, bars, a.status, kSiteEmpty))
-            break;
-          tc::fence_after_sync();
+          const uint32_t acc = tmem + (uint32_t)(ps * 2 * D);
           for (int kb = 0; kb < nk_proj; ++kb) {
             const int g = ps * nk_proj + kb;
             const int s = g % Cfg::SP;
@@ -391,11 +396,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t pb = pa + Cfg::kProjA;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              tc::mma_ss(tmem, tc::sdesc_sw128(pa + kk * 32, 16, 1024),
+              tc::mma_ss(acc, tc::sdesc_sw128(pa + kk * 32, 16, 1024),
                          tc::sdesc_sw128(pb + kk * 2048, 8192, 1024), idesc, (kb | kk) != 0);
             tc::mma_commit(&bars->pr_empty[s]);
           }
-          tc::mma_commit(&bars->pr_done);
+          tc::mma_commit(&bars->pr_done[ps]);
         }
         tc::mma_commit(&bars->pr_all);  // arrives once every MMA above has completed
       }
@@ -482,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (a) projection epilogue per pass: half 0 takes the K columns, half 1
     //     the V columns; round, write into the stationary tile, append.
     for (int ps = 0; ps < npass; ++ps) {
-      const bool ok = warp_wait(&bars->pr_done, ps & 1, bars, a.status, kSiteFull);
+      const bool ok = warp_wait(&bars->pr_done[ps], 0, bars, a.status, kSiteFull);
       tc::fence_after_sync();
       if (!ok) break;
       const int r = (pass0 + ps) * 128 + row;  // key row within the chunk
@@ -490,13 +495,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool mine = r >= nhost;            // this row is a new key projected here
       const bool append = mine && key < S && tg == 0;  // appended once per chunk
       uint8_t* tile = hh ? vs : ks;
+      C* const host_kv = static_cast<C*>(hh ? a.v_host : a.k_host);
       // (the row is looked up only where it exists: key < S)
-      C* host = append ? static_cast<C*>(hh ? a.v_host : a.k_host) + a.lay.row(b, kvh, key, D)
-                       : nullptr;
+      C* host = (kE4M3<C> && append) ? host_kv + a.lay.row(b, kvh, key, D) : nullptr;
 #pragma unroll 1
       for (int part = 0; part < D / 32; ++part) {
         uint32_t v[32];
-        tc::tmem_ld32(tmem + lane_off + hh * D + part * 32, v);
+        tc::tmem_ld32(tmem + lane_off + (uint32_t)(ps * 2 * D + hh * D + part * 32), v);
         tc::tmem_wait_ld();
         if constexpr (kE4M3<C>) {
           // the fp32 sums rounded once to E4M3 (nearest, saturating) are the
@@ -527,13 +532,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 4; ++q) {
             const uint4 o = pack8<T>(v + q * 8, 1.f);
             if (mine) *reinterpret_cast<uint4*>(tile + swz(r, part * 4 + q, kRegKV)) = o;
-            if (append) *reinterpret_cast<uint4*>(host + part * 32 + q * 8) = o;  // the append
           }
         }
       }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->pr_drain);
+      if constexpr (!kE4M3<C>) {
+        // the append, from the tile once the half's four warps have written
+        // the pass: consecutive threads take consecutive 16-byte pieces of a
+        // row, so each warp writes whole 128-byte lines of the host cache (a
+        // thread per row would leave every line to eight partial writes)
+        if (tg == 0) {
+          if (!warps_sync(&bars->ap_sync[hh][ps], 0, bars, a.status)) break;
+          constexpr int CPR = D / 8;  // 16-byte pieces per row
+          const int lo = max(nhost, (pass0 + ps) * 128);
+          const int hi = min((pass0 + ps + 1) * 128, nkeys);
+          const int ht = ((warp - 2) % 4) * 32 + lane;  // thread of the half
+          for (int i = ht; i < (hi - lo) * CPR; i += 128) {
+            const int rr = lo + i / CPR, cc = i % CPR;
+            *reinterpret_cast<uint4*>(host_kv + a.lay.row(b, kvh, k0 + rr, D) + cc * 8) =
+                *reinterpret_cast<const uint4*>(tile + swz(rr, cc, kRegKV));
+          }
+        }
+      }
     }
     // the host rows have landed (loader's cp.async tracked by kv_host)
     wait_or_abort(&bars->kv_host, 0, bars, a.status, kSiteFull);
