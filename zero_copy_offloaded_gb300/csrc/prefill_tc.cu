@@ -172,6 +172,22 @@ __device__ __forceinline__ uint4 pack8(const uint32_t* r, float mul) {
   return o;
 }
 
+// pack8 with the multiply two lanes per instruction (the same products)
+template <typename T>
+__device__ __forceinline__ uint4 pack8_x2(const uint32_t* r, float mul) {
+  const unsigned long long m2 = tc::f2_pack(mul, mul);
+  uint32_t h[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float lo, hi;
+    tc::f2_unpack(tc::f2_mul(tc::f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                             m2),
+                  lo, hi);
+    h[i] = tc::pack2<T>(lo, hi);
+  }
+  return make_uint4(h[0], h[1], h[2], h[3]);
+}
+
 // Cache element C: the activation type T, or 8-bit E4M3 (bf16 activations).
 // E4M3 rows of the host cache land in a staging slot of the stationary tile
 // (the part of row r that the converted row r overwrites last) and are
@@ -696,22 +712,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (pc == 0) mx = piece_max();
         uint32_t w[32];
         float ls8[8];
+        // (two keys per instruction: s*scale - m and the sums as fp32 pairs;
+        // the sums ls8[2q], ls8[2q + 1] are pair q of the accumulators)
         auto weights = [&]() {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) ls8[q] = 0.f;
+          const unsigned long long sc2 = tc::f2_pack(scale, scale), nm2 = tc::f2_pack(-mx, -mx);
+          unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};  // +0.0f pairs
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int k2 = pc * 64 + 2 * e;
-            float p0 = tc::ex2_approx(fmaf(__uint_as_float(r[2 * e]), scale, -mx));
-            float p1 = tc::ex2_approx(fmaf(__uint_as_float(r[2 * e + 1]), scale, -mx));
+            float p0, p1;
+            tc::f2_unpack(tc::f2_fma(tc::f2_pack(__uint_as_float(r[2 * e]),
+                                                 __uint_as_float(r[2 * e + 1])),
+                                     sc2, nm2),
+                          p0, p1);
+            p0 = tc::ex2_approx(p0);
+            p1 = tc::ex2_approx(p1);
             if (!full) {
               p0 = k2 < nvis ? p0 : 0.f;
               p1 = k2 + 1 < nvis ? p1 : 0.f;
             }
             w[e] = tc::pack2<__half>(p0, p1);
-            ls8[(2 * e) % 8] += p0;
-            ls8[(2 * e + 1) % 8] += p1;
+            acc[e % 4] = tc::f2_add(acc[e % 4], tc::f2_pack(p0, p1));
           }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tc::f2_unpack(acc[q], ls8[2 * q], ls8[2 * q + 1]);
         };
         weights();
         if (pc > 0) {
@@ -767,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
 #pragma unroll
       for (int q = 0; q < D / 8; ++q)
-        *reinterpret_cast<uint4*>(os + swz(row, q, kRegQ)) = pack8<__half>(o + q * 8, inv);
+        *reinterpret_cast<uint4*>(os + swz(row, q, kRegQ)) = pack8_x2<__half>(o + q * 8, inv);
       if (t < a.T) a.part_lse[blk * TG + (size_t)t * G + row % G] = mx + log2f(l);
       tc::fence_proxy_async_smem();
       __syncwarp();
