@@ -128,6 +128,7 @@ struct TcArgs {
   // chunk (tile_groups = 1); the naive baseline gives each CTA one group of
   // tiles_per_group tiles, so the chunk is fetched once per group.
   int tile_groups, tiles_per_group;
+  int new_first;  // fused prefill: launch the units holding new tokens first
   int debug_withhold;  // test hook: the loader never signals the chunk's host rows
   CacheLayout lay;  // rows of the caches (dense or paged)
   float scale_log2;
@@ -223,6 +224,42 @@ __device__ __forceinline__ uint4 e4m3x8_to(uint2 w) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// CTA u's unit: (b, KV head, Q tile group, chunk), chunks fastest.  That is
+// the order in which a Q-stationary kernel would stream them (the naive
+// baseline), and the fused prefill's order unless new_first.
+// Where the units holding new tokens fit in one wave (new_first), they run
+// first.  They are the longest (their projection comes before their tiles),
+// so they stay out of the last wave; they read no cached rows, so fewer CTAs
+// of the first wave queue for the link; and their unequal lengths stagger the
+// starts of the prefix units after them.  Within each part the units run
+// (b, KV head)-major with the chunks ascending, so that the units resident at
+// one time share a KV head's Q tiles in L2.
+__device__ __forceinline__ void unit_of(int u, const TcArgs& a, int& c, int& tg, int& bh) {
+  if (a.tile_groups != 1 || !a.new_first) {
+    c = u % a.nchunks;
+    tg = (u / a.nchunks) % a.tile_groups;
+    bh = u / (a.nchunks * a.tile_groups);
+    return;
+  }
+  tg = 0;
+  int n1 = 0;  // units holding new tokens (chunk >= the one holding key len[b])
+  for (int b = 0; b < a.B; ++b) n1 += a.Hkv * (a.nchunks - min(a.len[b] / kC, a.nchunks));
+  const bool first = u < n1;
+  int r = first ? u : u - n1;
+  for (int b = 0; b < a.B; ++b) {
+    const int cn = min(a.len[b] / kC, a.nchunks);  // first chunk with a new key
+    const int n = first ? a.nchunks - cn : cn;     // this part's chunks per KV head
+    if (r < a.Hkv * n) {
+      bh = b * a.Hkv + r / n;
+      c = (first ? cn : 0) + r % n;
+      return;
+    }
+    r -= a.Hkv * n;
+  }
+  bh = 0;
+  c = a.nchunks;  // not reached for u < B * Hkv * nchunks; a chunk past every key exits
+}
+
 template <typename T, typename C, int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q,
@@ -254,12 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(smem + Cfg::kOffBar);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // unit: (b, KV head, chunk) for the fused prefill; (b, KV head, Q tile
-  // group, chunk) with the chunks fastest for the naive baseline, the order in
-  // which a Q-stationary kernel would stream them
-  const int c = blockIdx.x % a.nchunks;
-  const int tg = (blockIdx.x / a.nchunks) % a.tile_groups;
-  const int bh = blockIdx.x / (a.nchunks * a.tile_groups);
+  int c, tg, bh;
+  unit_of(blockIdx.x, a, c, tg, bh);
   const int kvh = bh % a.Hkv, b = bh / a.Hkv;
   const int P = a.len[b];
   const int S = P + a.T;
@@ -956,6 +989,18 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, const void* wq,
   a.tiles_per_group = p.naive ? 1 : tiles;
   a.debug_withhold = p.debug_withhold;
   a.tile_groups = p.naive ? tiles : 1;
+  // New-token units first where they fit in one wave of CTAs (one per SM).
+  // Otherwise (many new chunks against the prefix: the fp16 MHA prefill has
+  // a quarter of its units new) the link would idle while wave after wave
+  // only projects, and the plain order, which mixes the two kinds, is faster.
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidValue;
+  long long nnew = 0;
+  for (int b = 0; b < p.B; ++b)
+    nnew += (long long)p.Hkv * (p.nchunks - std::min(p.len[b] / kC, p.nchunks));
+  a.new_first = !p.naive && nnew <= sms;
   for (int i = 0; i < kMaxBatch; ++i) a.len[i] = p.len[i];
 #define DKV_TC(TT, DD, GG) \
   if (D == DD && G == GG) e = launch_t<TT, TT, DD, GG>(a, mq, mx, mk, mv, p.out, s, timer); else
