@@ -129,6 +129,8 @@ struct TcArgs {
   // tiles_per_group tiles, so the chunk is fetched once per group.
   int tile_groups, tiles_per_group;
   int new_first;  // fused prefill: launch the units holding new tokens first
+  int nsplit;     // with new_first: the last nsplit prefix units run as two
+                  // CTAs each, one per half of the chunk's Q tiles
   int debug_withhold;  // test hook: the loader never signals the chunk's host rows
   CacheLayout lay;  // rows of the caches (dense or paged)
   float scale_log2;
@@ -233,8 +235,12 @@ __device__ __forceinline__ uint4 e4m3x8_to(uint2 w) {
 // of the first wave queue for the link; and their unequal lengths stagger the
 // starts of the prefix units after them.  Within each part the units run
 // (b, KV head)-major with the chunks ascending, so that the units resident at
-// one time share a KV head's Q tiles in L2.
-__device__ __forceinline__ void unit_of(int u, const TcArgs& a, int& c, int& tg, int& bh) {
+// one time share a KV head's Q tiles in L2.  The last nsplit prefix units
+// run as two CTAs each (half of the Q tiles each, the chunk fetched by both),
+// so that the last wave ends in shorter pieces.  tpg: Q tiles per CTA.
+__device__ __forceinline__ void unit_of(int u, const TcArgs& a, int& c, int& tg, int& bh,
+                                        int& tpg) {
+  tpg = a.tiles_per_group;
   if (a.tile_groups != 1 || !a.new_first) {
     c = u % a.nchunks;
     tg = (u / a.nchunks) % a.tile_groups;
@@ -242,10 +248,20 @@ __device__ __forceinline__ void unit_of(int u, const TcArgs& a, int& c, int& tg,
     return;
   }
   tg = 0;
-  int n1 = 0;  // units holding new tokens (chunk >= the one holding key len[b])
-  for (int b = 0; b < a.B; ++b) n1 += a.Hkv * (a.nchunks - min(a.len[b] / kC, a.nchunks));
+  int n1 = 0, n2 = 0;  // units holding new tokens (chunk >= the one holding key len[b]), others
+  for (int b = 0; b < a.B; ++b) {
+    const int cn = min(a.len[b] / kC, a.nchunks);
+    n1 += a.Hkv * (a.nchunks - cn);
+    n2 += a.Hkv * cn;
+  }
   const bool first = u < n1;
   int r = first ? u : u - n1;
+  if (!first && r >= n2 - a.nsplit) {  // a split unit: two consecutive CTAs
+    const int j = r - (n2 - a.nsplit);
+    r = n2 - a.nsplit + j / 2;
+    tg = j % 2;
+    tpg = (a.tiles_per_group + 1) / 2;
+  }
   for (int b = 0; b < a.B; ++b) {
     const int cn = min(a.len[b] / kC, a.nchunks);  // first chunk with a new key
     const int n = first ? a.nchunks - cn : cn;     // this part's chunks per KV head
@@ -291,8 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(smem + Cfg::kOffBar);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  int c, tg, bh;
-  unit_of(blockIdx.x, a, c, tg, bh);
+  int c, tg, bh, tpg;
+  unit_of(blockIdx.x, a, c, tg, bh, tpg);
   const int kvh = bh % a.Hkv, b = bh / a.Hkv;
   const int P = a.len[b];
   const int S = P + a.T;
@@ -304,10 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int pass0 = nhost / 128;               // first 128-row projection pass with new rows
   const int npass = has_new ? 2 - pass0 : 0;
   const int t_vis = max(0, k0 - P);            // first token that sees this chunk
-  const int tile0 = tg * a.tiles_per_group;    // this CTA's first Q tile of the chunk
+  const int tile0 = tg * tpg;                  // this CTA's first Q tile of the chunk
   if (tile0 * TQ >= a.T - t_vis) return;       // uniform, before any barrier
   const int t_lo = t_vis + tile0 * TQ;         // first token of this CTA's tiles
-  const int ntiles = min((a.T - t_lo + TQ - 1) / TQ, a.tiles_per_group);
+  const int ntiles = min((a.T - t_lo + TQ - 1) / TQ, tpg);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -940,7 +956,7 @@ cudaError_t launch_t(const TcArgs& args, const CUtensorMap& mq, const CUtensorMa
   if (!make_tmap_partial(&mpo, args.part_o, D, (uint64_t)args.T * G,
                          (uint64_t)args.nchunks * args.B * args.Hkv))
     return cudaErrorInvalidValue;
-  const int units = args.B * args.Hkv * args.nchunks * args.tile_groups;
+  const int units = args.B * args.Hkv * args.nchunks * args.tile_groups + args.nsplit;
   timer.before(s);
   k<<<units, kThreads, smem_request<D>(), s>>>(mq, mx, mk, mv, mpo, args);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1001,6 +1017,12 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, const void* wq,
   for (int b = 0; b < p.B; ++b)
     nnew += (long long)p.Hkv * (p.nchunks - std::min(p.len[b] / kC, p.nchunks));
   a.new_first = !p.naive && nnew <= sms;
+  // and, where a prefix unit is long (64 Q tiles or more), the last wave's
+  // worth of prefix units split in two.  Each split unit fetches its chunk
+  // twice (at most one more chunk per SM over the link) and waits for the
+  // cached rows twice, which a unit of a few dozen tiles does not repay.
+  const long long nprefix = (long long)p.B * p.Hkv * p.nchunks - nnew;
+  a.nsplit = a.new_first && tiles >= 64 ? (int)std::min<long long>(sms, nprefix) : 0;
   for (int i = 0; i < kMaxBatch; ++i) a.len[i] = p.len[i];
 #define DKV_TC(TT, DD, GG) \
   if (D == DD && G == GG) e = launch_t<TT, TT, DD, GG>(a, mq, mx, mk, mv, p.out, s, timer); else
