@@ -271,18 +271,21 @@ def test_prefill_llama8b_full_size_sampled_rows():
         case.free()
 
 
-@pytest.mark.parametrize("dtype,D", [("bf16", 64), ("fp16", 128)])
-def test_prefill_long_units_split_last_wave(dtype, D):
+@pytest.mark.parametrize("dtype,D,page_tokens", [("bf16", 64, 0), ("fp16", 128, 0),
+                                                 ("bf16", 128, 16)])
+def test_prefill_long_units_split_last_wave(dtype, D, page_tokens):
     """64 Q tiles per chunk (T = 2048, G = 4) with ragged prefixes: the units
     holding new tokens fit in one wave and run first, and the prefix units
     (fewer than one wave here) all run as two CTAs each, one per half of the
-    chunk's Q tiles.  Every output row and appended row against the oracle."""
+    chunk's Q tiles; dense and paged caches.  Every output row and appended
+    row against the oracle."""
     w = wl.Workload("t", "prefill", B=2, H=128, Hq=8, Hkv=2, D=D, P=1024, T=2048, dtype=dtype,
-                    kv_dist="uniform2" if dtype == "fp16" else "normal", seed=77)
-    case = Case(w, lens=[1024, 300], s_max=1024 + 2048 + 3)
+                    kv_dist="uniform2" if dtype == "fp16" else "normal", seed=77 + page_tokens)
+    case = Case(w, lens=[1024, 300], s_max=1024 + 2048 + 3, page_tokens=page_tokens)
     try:
         out = case.run_prefill()
-        check_prefill(case, out, case.oracle(), f"long units, split last wave {dtype} D={D}")
+        check_prefill(case, out, case.oracle(),
+                      f"long units, split last wave {dtype} D={D} pages={page_tokens}")
     finally:
         case.free()
 
